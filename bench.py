@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark: MoE dispatch + combine, microseconds per layer, on one GB300.
+
+One step = one MoE layer's hot path over one batch of synthetic tokens:
+(route +) count + scan (one fused kernel) -> dispatch pack/scatter -> [expert
+stand-in, untimed] -> combine. The timed value is the device time of the
+layout + dispatch + combine kernels (CUDA events on the launching stream), with
+L2 flushed (a 320 MB write) before the dispatch phase and again before the
+combine phase of every step, so every phase starts cold.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|...]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Under torchrun (N > 1) every rank runs an independent replica (the path has no
+cross-GPU exchange on one GPU per box) and rank 0 prints the max over ranks.
+Prints ONE JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine us/layer (effective HBM GB/s vs GB300 peak in roofline)"
+KERNEL_SOURCES = {"k_layout": "layout.cu", "k_dispatch_bf16": "dispatch.cu",
+                  "k_dispatch_fp8": "dispatch.cu", "k_combine": "combine.cu"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_init(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.12)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[3:7]):
+                if p.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# measured peaks and committed ncu traffic
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_sha(kernel: str) -> str:
+    src = os.path.join(ROOT, "combine_top_histogram_gb300", "csrc", KERNEL_SOURCES[kernel])
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current source of that kernel for this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    ent = tab.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_sha") != source_sha(kernel):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def oracle_layer_seconds(wl, budget_s: float, max_layers: int = 50):
+    """Times the CPU oracle's route/layout + dispatch + combine (the expert
+    stand-in is run untimed) on a bounded sample of the workload: the same
+    per-token distribution with fewer tokens per rank when a full layer would
+    take too long. Returns (seconds per full layer, sample description, layers)."""
+    import numpy as np
+
+    import oracle
+    from combine_top_histogram_gb300 import workloads as W
+    elems = wl.T * wl.k * wl.H
+    scale = max(1.0, elems / 6.0e7)
+    tr = max(1, int(wl.Tr / scale))
+    sw = wl.scaled(wl.name + "_cpu_sample", Tr=tr)
+    if wl.cap:
+        sw = sw.scaled(sw.name, Tr=tr, cap=max(1, int(round(wl.cap * tr / wl.Tr))))
+    inp = W.make_inputs(sw)
+    fp8 = sw.dispatch_dtype == W.MOE_FP8_E4M3
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_layers and (time.perf_counter() - t_start) < budget_s or len(times) < 1:
+        t0 = time.perf_counter()
+        if inp.logits is not None:
+            ids, w = oracle.route_topk(inp.logits, sw.k)
+        else:
+            ids, w = inp.ids, inp.w
+        lay = oracle.layout(sw.P, sw.Tr, sw.E, sw.k, ids, sw.cap)
+        if fp8:
+            recv, sc, _ = oracle.dispatch_fp8(sw.P, sw.Tr, sw.E, sw.k, inp.x, w, ids, lay["inv"],
+                                              sw.rows_max)
+        else:
+            recv, _ = oracle.dispatch_bf16(sw.P, sw.Tr, sw.E, sw.k, inp.x, w, ids, lay["inv"],
+                                           sw.rows_max)
+        t1 = time.perf_counter()
+        if fp8:
+            y = oracle.expert_dequant_fp8(recv, sc)
+        else:
+            c = inp.expert_scale if inp.expert_scale is not None else np.ones(sw.E, np.float32)
+            y = oracle.expert_scale_bf16(sw.E, lay["expert_offset"], c, recv)
+        t2 = time.perf_counter()
+        oracle.combine(lay["inv"], w, y, sw.T, sw.k)
+        t3 = time.perf_counter()
+        times.append((t1 - t0) + (t3 - t2))
+    per_layer = statistics.median(times) * (wl.Tr / tr)
+    sample = (f"{len(times)} oracle layers of {sw.T} tokens ({tr} per rank, same config), "
+              f"scaled x{wl.Tr / tr:.2f} to {wl.T} tokens; single-threaded C, -O2")
+    return per_layer, sample, len(times), times
+
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return 0
+    per_step = []
+    desc = None
+    for i in range(args.warmup + args.steps):
+        s, desc, _, _ = oracle_layer_seconds(wl, budget_s=0.0, max_layers=1)
+        if i >= args.warmup:
+            per_step.append(s)
+    us = statistics.median(per_step) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 3), "unit": "us/layer",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us / 1e3, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.dispatch_dtype == 0 else "fp8_e4m3+bf16",
+        "data": "synthetic", "config": {"workload": wl.name},
+        "cpu_baseline": {"value": round(us, 3), "unit": "us/layer", "cores": 1,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(us, 3), "unit": "us/layer", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def run_ours(args, wl, rank, world, local):
+    import numpy as np
+    import torch
+
+    from combine_top_histogram_gb300 import MoeLayer, accounting
+    from combine_top_histogram_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    inp = W.make_inputs(wl)
+    layer = MoeLayer(wl.P, wl.Tr, wl.E, wl.k, wl.H, wl.dispatch_dtype, wl.cap, str(dev))
+    x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    routed = inp.logits is not None
+    if routed:
+        logits = torch.from_numpy(inp.logits).to(dev)
+        w = layer.w
+    else:
+        ids = torch.from_numpy(inp.ids).to(dev)
+        w = torch.from_numpy(inp.w).to(dev)
+    c = torch.from_numpy(inp.expert_scale).to(dev) if inp.expert_scale is not None else None
+    flush_buf = torch.empty(320 << 20, dtype=torch.uint8, device=dev)
+
+    def layout():
+        if routed:
+            layer.route_layout(logits, stream)
+        else:
+            layer.layout(ids, stream)
+
+    def step(ev, flush_before_combine=True, flush_before=True):
+        if flush_before:
+            flush_buf.zero_()
+        ev[0].record(stream)
+        layout()
+        ev[1].record(stream)
+        layer.dispatch(x, w, stream)
+        ev[2].record(stream)
+        layer.expert(c, stream)
+        if flush_before_combine:
+            flush_buf.zero_()
+        ev[3].record(stream)
+        layer.combine(w, stream)
+        ev[4].record(stream)
+
+    def new_events(n):
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+
+    for ev in new_events(args.warmup):
+        step(ev)
+    torch.cuda.synchronize(dev)
+
+    # cold: flush before each phase
+    evs = new_events(args.steps)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for ev in evs:
+            step(ev)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dis_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    com_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    step_ms = [a + b + d for a, b, d in zip(lay_ms, dis_ms, com_ms)]
+    mean_ms = statistics.fmean(step_ms)
+    mean_ms_all = max_over_ranks(mean_ms, world)
+
+    # warm: no flushes (a layer right after the previous one; L2 keeps what fits)
+    wevs = new_events(min(args.steps, 100))
+    for ev in wevs:
+        step(ev, flush_before_combine=False, flush_before=False)
+    torch.cuda.synchronize(dev)
+    warm_ms = statistics.fmean([e[0].elapsed_time(e[2]) + e[3].elapsed_time(e[4]) for e in wevs])
+
+    # end to end through the public API: pinned host inputs -> device, layer,
+    # result -> pinned host, copies inside the timed region
+    x_h = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    if routed:
+        r_h = [torch.from_numpy(inp.logits).pin_memory()]
+        r_d = [logits]
+    else:
+        r_h = [torch.from_numpy(inp.ids).pin_memory(), torch.from_numpy(inp.w).pin_memory()]
+        r_d = [ids, w]
+    out_h = torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory()
+    h2d = x_h.numel() * 2 + sum(t.numel() * t.element_size() for t in r_h)
+    d2h = out_h.numel() * 2
+    e2e_ms = []
+    eevs = new_events(min(args.steps, 50) + 3)
+    for i, ev in enumerate(eevs):
+        flush_buf.zero_()
+        ev[0].record(stream)
+        x.copy_(x_h, non_blocking=True)
+        for a, b in zip(r_d, r_h):
+            a.copy_(b, non_blocking=True)
+        layout()
+        layer.dispatch(x, w, stream)
+        ev[1].record(stream)
+        layer.expert(c, stream)
+        flush_buf.zero_()
+        ev[2].record(stream)
+        layer.combine(w, stream)
+        out_h.copy_(layer.out, non_blocking=True)
+        ev[3].record(stream)
+    torch.cuda.synchronize(dev)
+    for ev in eevs[3:]:
+        e2e_ms.append(ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]))
+    e2e_us = max_over_ranks(statistics.fmean(e2e_ms) * 1e3, world)
+
+    kept = int(layer.layout_view()["totals"][0].item())
+    kb = accounting.hbm_bytes(wl.P, wl.Tr, wl.E, wl.k, wl.H, layer.fp8, rows=kept, routed=routed)
+    pay = accounting.payload_bytes(wl.P, wl.Tr, wl.k, wl.H, layer.fp8, rows=kept)
+    means = {"k_layout": statistics.fmean(lay_ms),
+             ("k_dispatch_fp8" if layer.fp8 else "k_dispatch_bf16"): statistics.fmean(dis_ms),
+             "k_combine": statistics.fmean(com_ms)}
+    bytes_of = {"k_layout": kb.layout, "k_dispatch_fp8": kb.dispatch,
+                "k_dispatch_bf16": kb.dispatch, "k_combine": kb.combine}
+    dom = max(means, key=means.get)
+    peak, peak_kind = hbm_peak()
+    achieved = bytes_of[dom] / (means[dom] * 1e-3) / 1e9
+    traffic = committed_traffic(dom, wl.name)
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
+        s, desc, n, _ = oracle_layer_seconds(wl, args.cpu_seconds)
+        cpu = {"value": round(s * 1e6, 1), "unit": "us/layer", "cores": 1, "kind": "oracle",
+               "sample": desc}
+    value_us = mean_ms_all * 1e3
+    line = {
+        "metric": METRIC, "value": round(value_us, 3), "unit": "us/layer",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_ms_all, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3+bf16" if layer.fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "P": wl.P, "tokens_per_rank": wl.Tr, "E": wl.E,
+                   "top_k": wl.k, "hidden": wl.H, "capacity": wl.cap,
+                   "l2": "flushed (320 MB write) before the dispatch and the combine phase "
+                         "of every timed step",
+                   "replicas": world},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": bytes_of[dom]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "per_kernel_us": {k: round(v * 1e3, 3) for k, v in means.items()},
+        "assignments_per_s": round(world * wl.Na / (mean_ms_all * 1e-3), 1),
+        "effective_gbs": round((kb.layout + kb.dispatch + kb.combine) / (mean_ms_all * 1e-3) / 1e9, 1),
+        "payload_gbs": round(pay["total"] / (mean_ms_all * 1e-3) / 1e9, 1),
+        "warm_us_per_layer": round(warm_ms * 1e3, 3),
+        "kept_rows": kept,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    from combine_top_histogram_gb300 import workloads as W
+    if args.config not in W.CONFIGS:
+        raise SystemExit(f"unknown --config {args.config}; choose from {list(W.CONFIGS)}")
+    wl = W.CONFIGS[args.config]
+    rank, world, local = dist_init(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, wl, rank, world)
+        return run_ours(args, wl, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

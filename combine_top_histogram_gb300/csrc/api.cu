@@ -1,0 +1,357 @@
+// api.cu -- the C ABI of libmoe_ep.so: argument checks, workspace carving,
+// call-order state, and kernel launches. See include/moe_ep.h for the
+// contract of every entry point.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "internal.cuh"
+#include "moe_ep.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->num_ranks < 1 || c->tokens_per_rank < 1 || c->num_experts < 1 || c->top_k < 1 ||
+      c->hidden < 1 || c->expert_capacity < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->num_experts % c->num_ranks != 0) return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
+  if (c->dispatch_dtype != MOE_BF16 && c->dispatch_dtype != MOE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+  if (c->combine_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->num_experts > MOE_MAX_EXPERTS || c->top_k > MOE_MAX_TOPK || c->num_ranks > MOE_MAX_RANKS)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->hidden % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->dispatch_dtype == MOE_FP8_E4M3 && c->hidden % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  const long long T = (long long)c->num_ranks * c->tokens_per_rank;
+  if (T * c->top_k >= (1ll << 31) - 1) return MOE_ERR_UNSUPPORTED;  // int32 row indices
+  return MOE_OK;
+}
+
+struct Plan {
+  int tpc_route, cps_route, tpc_ids, cps_ids, nchunks_max;
+  size_t off_ctrl, off_totals, off_n_raw, off_n_kept, off_eoff, off_cnt, off_kept, off_C,
+      off_send, off_recv, off_rank, off_hist, off_acode, off_inv, bytes;
+};
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Chunking of the layout kernel. Given ids, a chunk of ~2048 assignments
+// keeps the scan short; when routing, chunks are cut smaller so the top-k
+// work (one warp per token) spreads over about two CTAs per SM.
+Plan make_plan(const moe_config_t* c, int num_sms) {
+  Plan p{};
+  const int P = c->num_ranks, Tr = c->tokens_per_rank, E = c->num_experts, k = c->top_k;
+  const long long T = (long long)P * Tr, Na = T * k;
+  const int max_tpc = moe::kMaxChunkAssign / k;
+  int tpc = 2048 / k;
+  if (tpc < 1) tpc = 1;
+  if (tpc > max_tpc) tpc = max_tpc;
+  if (tpc > Tr) tpc = Tr;
+  p.tpc_ids = tpc;
+  p.cps_ids = ceil_div(Tr, tpc);
+  int tr = (int)((T + 2ll * num_sms - 1) / (2ll * num_sms));
+  if (tr < moe::kLayoutWarps) tr = moe::kLayoutWarps;
+  if (tr > 2048 / k) tr = 2048 / k;
+  if (tr < 1) tr = 1;
+  if (tr > max_tpc) tr = max_tpc;
+  if (tr > Tr) tr = Tr;
+  p.tpc_route = tr;
+  p.cps_route = ceil_div(Tr, tr);
+  const int n1 = P * p.cps_ids, n2 = P * p.cps_route;
+  p.nchunks_max = n1 > n2 ? n1 : n2;
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  p.off_ctrl = take(64);
+  p.off_totals = take(4 * sizeof(int32_t));
+  p.off_n_raw = take((size_t)E * 4);
+  p.off_n_kept = take((size_t)E * 4);
+  p.off_eoff = take((size_t)(E + 1) * 4);
+  p.off_cnt = take((size_t)P * E * 4);
+  p.off_kept = take((size_t)P * E * 4);
+  p.off_C = take((size_t)P * P * 4);
+  p.off_send = take((size_t)P * P * 4);
+  p.off_recv = take((size_t)P * E * 4);
+  p.off_rank = take((size_t)(P + 1) * 4);
+  p.off_hist = take((size_t)p.nchunks_max * E * 4);
+  p.off_acode = take((size_t)Na * 4);
+  p.off_inv = take((size_t)Na * 4);
+  p.bytes = off;
+  return p;
+}
+
+int query_sms(int* device, int* sms) {
+  if (cudaGetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe::LayoutArgs layout_args(moe_handle_t h, bool route) {
+  moe::LayoutArgs a{};
+  a.acode = h->acode;
+  a.hist = h->hist;
+  a.n_raw = h->n_raw;
+  a.n_kept = h->n_kept;
+  a.expert_offset = h->expert_offset;
+  a.cnt = h->cnt;
+  a.kept_cnt = h->kept_cnt;
+  a.C = h->C;
+  a.send_offset = h->send_offset;
+  a.recv_offset = h->recv_offset;
+  a.rank_base = h->rank_base;
+  a.totals = h->totals;
+  a.status = h->status;
+  a.done = h->done;
+  a.P = h->cfg.num_ranks;
+  a.E = h->cfg.num_experts;
+  a.k = h->cfg.top_k;
+  a.L = h->L;
+  a.Tr = h->cfg.tokens_per_rank;
+  a.tpc = route ? h->tpc_route : h->tpc_ids;
+  a.cps = route ? h->cps_route : h->cps_ids;
+  a.nchunks = a.P * a.cps;
+  a.cap = h->cfg.expert_capacity;
+  a.Na = h->Na;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  int dev = 0, sms = 0;
+  if (query_sms(&dev, &sms) != MOE_OK) sms = 152;
+  return make_plan(cfg, sms).bytes;
+}
+
+int64_t moe_recv_rows_max(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  const long long Na = (long long)cfg->num_ranks * cfg->tokens_per_rank * cfg->top_k;
+  if (cfg->expert_capacity > 0) {
+    const long long ec = (long long)cfg->num_experts * cfg->expert_capacity;
+    return ec < Na ? ec : Na;
+  }
+  return Na;
+}
+
+int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
+                      moe_handle_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate(cfg);
+  if (rc != MOE_OK) return rc;
+  if (!d_workspace) return MOE_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  rc = query_sms(&dev, &sms);
+  if (rc != MOE_OK) return rc;
+  const Plan p = make_plan(cfg, sms);
+  if (bytes < p.bytes || !aligned(d_workspace, kAlign)) return MOE_ERR_WORKSPACE;
+  // Opt in to the layout kernel's shared memory for the larger chunking.
+  const int tpc_max = p.tpc_route > p.tpc_ids ? p.tpc_route : p.tpc_ids;
+  if (moe::layout_prepare(cfg->num_experts, tpc_max, cfg->top_k) != cudaSuccess) return MOE_ERR_CUDA;
+
+  moe_handle* h = static_cast<moe_handle*>(calloc(1, sizeof(moe_handle)));
+  if (!h) return MOE_ERR_INVALID_ARG;
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = sms;
+  h->T = (long long)cfg->num_ranks * cfg->tokens_per_rank;
+  h->Na = h->T * cfg->top_k;
+  h->rows_max = moe_recv_rows_max(cfg);
+  h->L = cfg->num_experts / cfg->num_ranks;
+  h->tpc_route = p.tpc_route;
+  h->cps_route = p.cps_route;
+  h->tpc_ids = p.tpc_ids;
+  h->cps_ids = p.cps_ids;
+  h->nchunks_max = p.nchunks_max;
+  char* ws = static_cast<char*>(d_workspace);
+  h->ws = ws;
+  h->ws_bytes = bytes;
+  h->status = reinterpret_cast<uint32_t*>(ws + p.off_ctrl);
+  h->done = h->status + 1;
+  h->totals = reinterpret_cast<int32_t*>(ws + p.off_totals);
+  h->n_raw = reinterpret_cast<int32_t*>(ws + p.off_n_raw);
+  h->n_kept = reinterpret_cast<int32_t*>(ws + p.off_n_kept);
+  h->expert_offset = reinterpret_cast<int32_t*>(ws + p.off_eoff);
+  h->cnt = reinterpret_cast<int32_t*>(ws + p.off_cnt);
+  h->kept_cnt = reinterpret_cast<int32_t*>(ws + p.off_kept);
+  h->C = reinterpret_cast<int32_t*>(ws + p.off_C);
+  h->send_offset = reinterpret_cast<int32_t*>(ws + p.off_send);
+  h->recv_offset = reinterpret_cast<int32_t*>(ws + p.off_recv);
+  h->rank_base = reinterpret_cast<int32_t*>(ws + p.off_rank);
+  h->hist = reinterpret_cast<int32_t*>(ws + p.off_hist);
+  h->acode = reinterpret_cast<int32_t*>(ws + p.off_acode);
+  h->inv = reinterpret_cast<int32_t*>(ws + p.off_inv);
+  if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess) {
+    free(h);
+    return MOE_ERR_CUDA;
+  }
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_handle_destroy(moe_handle_t h) {
+  free(h);
+  return MOE_OK;
+}
+
+int moe_route_topk(moe_handle_t h, const float* logits, int32_t* ids, float* w, void* stream) {
+  if (!h || !logits || !ids || !w) return MOE_ERR_INVALID_ARG;
+  return cuda_rc(moe::launch_route_only(logits, ids, w, h->T, h->cfg.num_experts, h->cfg.top_k,
+                                        h->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+static int run_layout(moe_handle_t h, bool route, const int32_t* ids_in, const float* logits,
+                      int32_t* ids_out, float* w_out, void* stream) {
+  moe::LayoutArgs a = layout_args(h, route);
+  a.ids_in = ids_in;
+  a.logits = logits;
+  a.ids_out = ids_out;
+  a.w_out = w_out;
+  const int rc = cuda_rc(moe::launch_layout(a, route, h->num_sms, static_cast<cudaStream_t>(stream)));
+  if (rc != MOE_OK) return rc;
+  h->cur_tpc = a.tpc;
+  h->cur_cps = a.cps;
+  h->layout_gen += 1;
+  return MOE_OK;
+}
+
+int moe_dispatch_layout(moe_handle_t h, const int32_t* ids, void* stream) {
+  if (!h || !ids) return MOE_ERR_INVALID_ARG;
+  return run_layout(h, false, ids, nullptr, nullptr, nullptr, stream);
+}
+
+int moe_route_dispatch_layout(moe_handle_t h, const float* logits, int32_t* ids, float* w,
+                              void* stream) {
+  if (!h || !logits || !ids || !w) return MOE_ERR_INVALID_ARG;
+  return run_layout(h, true, nullptr, logits, ids, w, stream);
+}
+
+int moe_get_layout(moe_handle_t h, moe_layout_view_t* out) {
+  if (!h || !out) return MOE_ERR_INVALID_ARG;
+  out->expert_count = h->n_kept;
+  out->expert_count_raw = h->n_raw;
+  out->expert_offset = h->expert_offset;
+  out->src_expert_count = h->cnt;
+  out->src_expert_kept = h->kept_cnt;
+  out->count_matrix = h->C;
+  out->send_offset = h->send_offset;
+  out->recv_offset = h->recv_offset;
+  out->rank_base = h->rank_base;
+  out->inv = h->inv;
+  out->totals = h->totals;
+  return MOE_OK;
+}
+
+int moe_dispatch(moe_handle_t h, const void* x, const float* w, void* recv_x, float* recv_scale,
+                 const moe_recv_meta_t* meta, void* stream) {
+  if (!h || !x || !w || !recv_x || !meta) return MOE_ERR_INVALID_ARG;
+  if (!meta->local_expert || !meta->src_rank || !meta->src_token || !meta->slot || !meta->weight)
+    return MOE_ERR_INVALID_ARG;
+  const bool fp8 = h->cfg.dispatch_dtype == MOE_FP8_E4M3;
+  if (fp8 && !recv_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv_x, 16)) return MOE_ERR_INVALID_ARG;
+  if (h->layout_gen == 0) return MOE_ERR_STATE;
+  moe::DispatchArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.w = w;
+  a.acode = h->acode;
+  a.hist = h->hist;
+  a.expert_offset = h->expert_offset;
+  a.inv = h->inv;
+  a.recv = recv_x;
+  a.recv_scale = recv_scale;
+  a.m_local_expert = meta->local_expert;
+  a.m_src_rank = meta->src_rank;
+  a.m_src_token = meta->src_token;
+  a.m_slot = meta->slot;
+  a.m_weight = meta->weight;
+  a.T = h->T;
+  a.Tr = h->cfg.tokens_per_rank;
+  a.k = h->cfg.top_k;
+  a.E = h->cfg.num_experts;
+  a.L = h->L;
+  a.H = h->cfg.hidden;
+  a.tpc = h->cur_tpc;
+  a.cps = h->cur_cps;
+  a.cap = h->cfg.expert_capacity;
+  const int rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
+  if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
+  return rc;
+}
+
+int moe_expert_standin(moe_handle_t h, const void* recv_x, const float* recv_scale,
+                       const float* expert_scale, void* y, void* stream) {
+  if (!h || !recv_x || !y) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = h->cfg.dispatch_dtype == MOE_FP8_E4M3;
+  if (fp8 && !recv_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(recv_x, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  if (h->dispatch_gen == 0 || h->dispatch_gen != h->layout_gen) return MOE_ERR_STATE;
+  moe::StandinArgs a{};
+  a.recv = recv_x;
+  a.recv_scale = recv_scale;
+  a.expert_scale = expert_scale;
+  a.expert_offset = h->expert_offset;
+  a.y = static_cast<uint16_t*>(y);
+  a.rows_max = h->rows_max;
+  a.E = h->cfg.num_experts;
+  a.H = h->cfg.hidden;
+  a.fp8 = fp8 ? 1 : 0;
+  return cuda_rc(moe::launch_standin(a, h->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine(moe_handle_t h, const void* y, const float* w, void* out, void* stream) {
+  if (!h || !y || !w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (h->dispatch_gen == 0 || h->dispatch_gen != h->layout_gen) return MOE_ERR_STATE;
+  moe::CombineArgs a{};
+  a.y = static_cast<const uint16_t*>(y);
+  a.w = w;
+  a.inv = h->inv;
+  a.out = static_cast<uint16_t*>(out);
+  a.T = h->T;
+  a.k = h->cfg.top_k;
+  a.H = h->cfg.hidden;
+  return cuda_rc(moe::launch_combine(a, h->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_read_status(moe_handle_t h, uint32_t* flags, void* stream) {
+  if (!h || !flags) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(flags, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(h->status, 0, sizeof(uint32_t)) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+const char* moe_error_string(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or dtype";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_STATE: return "call order violated";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"

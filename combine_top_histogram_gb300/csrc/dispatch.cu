@@ -1,0 +1,195 @@
+// dispatch.cu -- permute + pack + all-to-all-v scatter, with optional fused
+// FP8 e4m3 quantisation (per token and 128-channel block, fp32 scale).
+//
+// Pages: "[Infra-10] All-to-All Optimization", 4.3 (write the permutation
+// straight into the destination-contiguous communication buffer, no temporary
+// permutation buffer), 5.1 (one pass writes hidden states, token index and
+// routing weight), 5.2 (destination segments bucketed by local expert; the
+// network output buffer is the expert kernel's input), 4.1 (FP8 on the wire
+// with scale metadata); "Expert Parallel: MoE Token ...", payload schema and
+// the bijection (every valid assignment sent exactly once);
+// "Efficient and portable MoE communication", "Dispatch" (block scale
+// factors travel with the tokens).
+//
+// One GPU: the P virtual ranks' receive segments are ranges of one receive
+// buffer, so "sending" an assignment is storing its row at its receive row.
+// Each CTA takes one token at a time: reads the bf16 row from HBM once into
+// registers (16-byte loads, coalesced), quantises it once if FP8, and stores
+// it to each of the token's k receive rows (16- or 8-byte stores, coalesced).
+// The receive row of slot j is
+//     r = expert_offset[e] + chunk_base[chunk][e] + chunk-local rank
+// (the stable (expert, source, token, slot) order) and is kept iff its
+// in-expert position is below the capacity.
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kDispatchThreads = 128;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  // x is read exactly once: do not keep it in L1.
+  return __ldlu(p);
+}
+
+// Resolves the k receive rows of token g into rows_s, writes inv and the row
+// metadata. Threads 0..k-1 each take one slot.
+__device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g, int* rows_s) {
+  const int j = threadIdx.x;
+  if (j >= p.k) return;
+  const long long a = g * p.k + j;
+  const int code = __ldg(p.acode + a);
+  int r = -1;
+  if (code >= 0) {
+    const int e = code_expert(code);
+    const int s = (int)(g / p.Tr);
+    const int t = (int)(g - (long long)s * p.Tr);
+    const int b = s * p.cps + t / p.tpc;
+    const int pos = __ldg(p.hist + (long long)b * p.E + e) + code_rank(code);
+    if (p.cap <= 0 || pos < p.cap) {
+      r = __ldg(p.expert_offset + e) + pos;
+      p.m_local_expert[r] = e % p.L;
+      p.m_src_rank[r] = s;
+      p.m_src_token[r] = t;
+      p.m_slot[r] = j;
+      p.m_weight[r] = __ldg(p.w + a);
+    }
+  }
+  p.inv[a] = r;
+  rows_s[j] = r;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(kDispatchThreads) k_dispatch_bf16(const DispatchArgs p) {
+  __shared__ int rows_s[MOE_MAX_TOPK];
+  const int nvec = p.H >> 3;  // 16-byte vectors per row
+  const int tid = threadIdx.x;
+  for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
+    resolve_rows(p, g, rows_s);
+    __syncthreads();
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
+    for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
+      uint4 val[VPT];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = v0 + i * kDispatchThreads + tid;
+        if (v < nvec) val[i] = ld_stream(src + v);
+      }
+      for (int j = 0; j < p.k; ++j) {
+        const int r = rows_s[j];
+        if (r < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.recv) + (long long)r * p.H);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = v0 + i * kDispatchThreads + tid;
+          if (v < nvec) dst[v] = val[i];
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t e4m3_byte(float v) {
+  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Quantises 8 bf16 values (one 16-byte vector) with scale s; returns 8 codes.
+__device__ __forceinline__ uint2 quant8(const uint4 x, float s, bool zero_block) {
+  if (zero_block) return make_uint2(0u, 0u);
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t c0 = e4m3_byte(__fdiv_rn(bf16_lo(w[q]), s));
+    const uint32_t c1 = e4m3_byte(__fdiv_rn(bf16_hi(w[q]), s));
+    out[q >> 1] |= (c0 | (c1 << 8)) << (16 * (q & 1));
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+__device__ __forceinline__ float amax8(const uint4 x) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  float m = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    m = fmaxf(m, fabsf(bf16_lo(w[q])));
+    m = fmaxf(m, fabsf(bf16_hi(w[q])));
+  }
+  return m;
+}
+
+// FP8: a 128-channel block is 16 consecutive vectors, held by 16 consecutive
+// lanes (blockDim and the vector stride are multiples of 16), so the block's
+// amax is a 4-step xor-shuffle reduction inside each half-warp.
+template <int VPT>
+__global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const DispatchArgs p) {
+  __shared__ int rows_s[MOE_MAX_TOPK];
+  const int nvec = p.H >> 3;
+  const int nblk = p.H >> 7;
+  const int tid = threadIdx.x;
+  for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
+    resolve_rows(p, g, rows_s);
+    __syncthreads();
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
+    for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
+      uint4 val[VPT];
+      float sc[VPT];
+      uint2 code[VPT];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = v0 + i * kDispatchThreads + tid;
+        val[i] = v < nvec ? ld_stream(src + v) : make_uint4(0u, 0u, 0u, 0u);
+        float m = amax8(val[i]);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        sc[i] = __fdiv_rn(m, 448.0f);
+        code[i] = quant8(val[i], sc[i], m == 0.0f);
+      }
+      for (int j = 0; j < p.k; ++j) {
+        const int r = rows_s[j];
+        if (r < 0) continue;
+        uint2* dst = reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.recv) + (long long)r * p.H);
+        float* sdst = p.recv_scale + (long long)r * nblk;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = v0 + i * kDispatchThreads + tid;
+          if (v < nvec) {
+            dst[v] = code[i];
+            if ((tid & 15) == 0) sdst[v >> 4] = sc[i];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st) {
+  if (a.T <= 0) return cudaSuccess;
+  long long blocks = a.T;
+  const long long cap = (long long)num_sms * 16;  // 16 CTAs of 128 threads fill an SM
+  if (blocks > cap) blocks = cap;
+  const int nvec = a.H >> 3;
+  if (fp8) {
+    if (nvec <= 128) k_dispatch_fp8<1><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+    else if (nvec <= 512) k_dispatch_fp8<4><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+    else k_dispatch_fp8<8><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+  } else {
+    if (nvec <= 128) k_dispatch_bf16<1><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+    else if (nvec <= 512) k_dispatch_bf16<4><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+    else k_dispatch_bf16<8><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

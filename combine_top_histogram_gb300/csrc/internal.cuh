@@ -1,0 +1,117 @@
+// internal.cuh -- shared declarations of the CUDA side of libmoe_ep.so:
+// the handle layout, kernel argument blocks and launcher prototypes.
+// Not installed; the public interface is include/moe_ep.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_ep.h"
+
+namespace moe {
+
+// Layout kernel shape: 16 warps per chunk; one warp routes one token at a time.
+constexpr int kLayoutThreads = 512;
+constexpr int kLayoutWarps = kLayoutThreads / 32;
+// Assignments per layout chunk are bounded so that a chunk-local rank fits in
+// the low 16 bits of an assignment code (code = expert << 16 | rank).
+constexpr int kMaxChunkAssign = 4096;
+
+// Per-assignment code written by the layout kernel and read by dispatch:
+// (expert << 16) | (stable rank of the assignment among the chunk's
+// assignments to that expert), or -1 for a masked slot.
+__host__ __device__ inline int code_expert(int c) { return c >> 16; }
+__host__ __device__ inline int code_rank(int c) { return c & 0xFFFF; }
+
+struct LayoutArgs {
+  const int32_t* ids_in;  // [T*k] given ids (layout-only mode)
+  const float* logits;    // [T*E] router logits (route mode)
+  int32_t* ids_out;       // [T*k] routed ids (route mode)
+  float* w_out;           // [T*k] routed weights (route mode)
+  int32_t* acode;         // [T*k] assignment codes
+  int32_t* hist;          // [nchunks*E]: chunk counts, then exclusive chunk bases
+  int32_t* n_raw;         // [E]
+  int32_t* n_kept;        // [E]
+  int32_t* expert_offset; // [E+1]
+  int32_t* cnt;           // [P*E]
+  int32_t* kept_cnt;      // [P*E]
+  int32_t* C;             // [P*P]
+  int32_t* send_offset;   // [P*P]
+  int32_t* recv_offset;   // [P*E]
+  int32_t* rank_base;     // [P+1]
+  int32_t* totals;        // [4]
+  uint32_t* status;
+  uint32_t* done;         // chunk arrival counter, reset by the last chunk
+  int P, E, k, L, Tr;
+  int tpc, cps, nchunks;  // tokens per chunk, chunks per source rank, chunks
+  int cap;                // 0 = unlimited
+  long long Na;
+};
+
+struct DispatchArgs {
+  const uint16_t* x;      // bf16 bits [T*H]
+  const float* w;         // [T*k]
+  const int32_t* acode;   // [T*k]
+  const int32_t* hist;    // [nchunks*E] exclusive chunk bases
+  const int32_t* expert_offset;
+  int32_t* inv;           // [T*k]
+  void* recv;             // bf16 [rows*H] or e4m3 [rows*H]
+  float* recv_scale;      // [rows*H/128] (FP8)
+  int32_t* m_local_expert;
+  int32_t* m_src_rank;
+  int32_t* m_src_token;
+  int32_t* m_slot;
+  float* m_weight;
+  long long T;
+  int Tr, k, E, L, H, tpc, cps, cap;
+};
+
+struct CombineArgs {
+  const uint16_t* y;      // bf16 [rows*H]
+  const float* w;         // [T*k]
+  const int32_t* inv;     // [T*k]
+  uint16_t* out;          // bf16 [T*H]
+  long long T;
+  int k, H;
+};
+
+struct StandinArgs {
+  const void* recv;        // bf16 or e4m3 [rows*H]
+  const float* recv_scale; // FP8 scales
+  const float* expert_scale; // [E] or null
+  const int32_t* expert_offset; // [E+1]
+  uint16_t* y;
+  long long rows_max;
+  int E, H, fp8;
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_layout(const LayoutArgs& a, bool route, int num_sms, cudaStream_t st);
+cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long long T,
+                              int E, int k, int num_sms, cudaStream_t st);
+size_t layout_smem_bytes(int E, int tpc, int k);
+cudaError_t layout_prepare(int E, int tpc, int k);
+cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_standin(const StandinArgs& a, int num_sms, cudaStream_t st);
+
+}  // namespace moe
+
+// Host-side handle: configuration plus pointers into the caller's workspace.
+struct moe_handle {
+  moe_config_t cfg;
+  int device;
+  int num_sms;
+  long long T, Na, rows_max;
+  int L;
+  int tpc_route, cps_route, tpc_ids, cps_ids, nchunks_max;
+  int cur_tpc, cur_cps;     // chunking of the most recent layout
+  char* ws;
+  size_t ws_bytes;
+  uint32_t* status;         // ctrl[0]
+  uint32_t* done;           // ctrl[1]
+  int32_t* totals;          // [4]
+  int32_t *n_raw, *n_kept, *expert_offset, *cnt, *kept_cnt, *C, *send_offset,
+      *recv_offset, *rank_base, *hist, *acode, *inv;
+  unsigned long long layout_gen, dispatch_gen;
+};

@@ -1,0 +1,83 @@
+"""One MoE layer's dispatch/combine buffers and calls, over the C ABI.
+
+``MoeLayer`` allocates (with torch) the workspace and the receive, metadata
+and output buffers sized by the library's worst-case rule, then runs the path
+through the binding: route+layout (or layout from given ids) -> dispatch ->
+expert stand-in -> combine. Convenience for tests, the benchmark and smoke
+checks; every step runs in the library's kernels.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+from . import binding as B
+
+
+class MoeLayer:
+    def __init__(self, P: int, Tr: int, E: int, k: int, H: int, dispatch_dtype: int = B.MOE_BF16,
+                 cap: int = 0, device: str = "cuda"):
+        import torch
+        self.P, self.Tr, self.E, self.k, self.H = P, Tr, E, k, H
+        self.T = P * Tr
+        self.fp8 = dispatch_dtype == B.MOE_FP8_E4M3
+        self.cfg = B.make_config(P, Tr, E, k, H, dispatch_dtype, cap)
+        self.handle = B.moe_handle_create(self.cfg, device=device)
+        self.rows = B.moe_recv_rows_max(self.cfg)
+        dev = torch.device(device)
+        rows, T = self.rows, self.T
+        if self.fp8:
+            self.recv_x = torch.empty((rows, H), dtype=torch.uint8, device=dev)
+            self.recv_scale = torch.empty((rows, H // 128), dtype=torch.float32, device=dev)
+        else:
+            self.recv_x = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+            self.recv_scale = None
+        self.meta = {
+            "local_expert": torch.empty(rows, dtype=torch.int32, device=dev),
+            "src_rank": torch.empty(rows, dtype=torch.int32, device=dev),
+            "src_token": torch.empty(rows, dtype=torch.int32, device=dev),
+            "slot": torch.empty(rows, dtype=torch.int32, device=dev),
+            "weight": torch.empty(rows, dtype=torch.float32, device=dev),
+        }
+        self.y = torch.empty((rows, H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
+
+    # -- steps ---------------------------------------------------------------
+    def route_layout(self, logits, stream=None):
+        """Fused top-k + count + scan; fills self.ids and self.w."""
+        B.moe_route_dispatch_layout(self.handle, logits, self.ids, self.w, stream)
+
+    def layout(self, ids, stream=None):
+        B.moe_dispatch_layout(self.handle, ids, stream)
+
+    def dispatch(self, x, w, stream=None):
+        B.moe_dispatch(self.handle, x, w, self.recv_x, self.recv_scale, self.meta, stream)
+
+    def expert(self, expert_scale=None, stream=None):
+        B.moe_expert_standin(self.handle, self.recv_x, self.recv_scale, expert_scale, self.y,
+                             stream)
+
+    def combine(self, w, stream=None):
+        B.moe_combine(self.handle, self.y, w, self.out, stream)
+
+    def forward(self, x, ids=None, w=None, logits=None, expert_scale=None, stream=None):
+        """Whole layer; with logits the routed ids/weights land in self.ids / self.w."""
+        if logits is not None:
+            self.route_layout(logits, stream)
+            w = self.w
+        else:
+            self.layout(ids, stream)
+        self.dispatch(x, w, stream)
+        self.expert(expert_scale, stream)
+        self.combine(w, stream)
+        return self.out
+
+    def layout_view(self) -> dict:
+        return B.moe_get_layout(self.handle)
+
+    def status(self, stream=None) -> int:
+        return B.moe_read_status(self.handle, stream)
+
+    def close(self):
+        self.handle.close()

@@ -1,0 +1,221 @@
+/*
+ * moe_ep.h -- C ABI of the single-GPU MoE expert-parallel dispatch/combine
+ * library (libmoe_ep.so, CUDA, sm_103a).
+ *
+ * The path: route -> count -> permute/pack -> all-to-all-v dispatch ->
+ * (expert) -> combine -> unpermute with the top-k weighted sum.
+ * Sources (page title, section):
+ *   [A2A]  "[Infra-10] All-to-All Optimization" (xutianle.me):
+ *          2 (two all-to-alls per MoE layer), 2.1 (payload carries expert id,
+ *          token index, weight, counts, scales), 3.5 (count -> prefix ->
+ *          scatter -> pack; unpack -> restore order -> weighted combine),
+ *          4.1 (FP8 on the wire), 4.3 (write straight into the
+ *          destination-contiguous buffer), 5.2 (segments per destination rank,
+ *          bucketed by local expert), 8.1 (capacity and dropping).
+ *   [EP]   "Expert Parallel: MoE Token ..." (charlestar.github.io):
+ *          "A Top-2 routing example", "Why count and permute before dispatch"
+ *          (owner(e), send_count, prefix sum -> send_offset, payload schema,
+ *          bijection), "All-to-All-v" (count matrix C_ij), "Combine is not
+ *          simply sending results back" (handle contents, stable token order),
+ *          "Memory is not only expert weights" (preallocate by the worst case).
+ *   [PPLX] "Efficient and portable MoE communication" (pplx-kernels blog):
+ *          introduction (router top-k, weighted average), "Dispatch" (block
+ *          scale factors), "Combine".
+ *
+ * One GPU holds P "virtual EP ranks". Rank s owns tokens [s*T_r, (s+1)*T_r)
+ * of the input and experts [s*L, (s+1)*L), L = E/P. The all-to-all-v is a
+ * device scatter into per-expert contiguous receive segments, driven by the
+ * count matrix the library builds on the device: no host sync, no second GPU,
+ * no collective.
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller
+ *     allocates and owns every buffer, including the workspace. The handle
+ *     holds only the configuration and pointers into the workspace.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
+ *     NULL = legacy default stream) and never synchronises the host, except
+ *     moe_read_status, which is for tests and debugging.
+ *   - Calls on one handle must be ordered on one stream (or ordered by the
+ *     caller with events); overlapping calls on one handle race on the
+ *     workspace.
+ *   - Host-checkable errors return a negative MOE_ERR_* code and enqueue
+ *     nothing. Data-dependent problems (for example an expert id outside
+ *     [-1, E)) set bits in the device status word and the offending slot is
+ *     treated as masked. Capacity drops are counted, not errors.
+ *   - Token rows are bf16 [T, H] row-major; T = P*T_r; global token
+ *     g = s*T_r + t; assignment a = g*k + j (slot j of token g).
+ */
+#ifndef MOE_EP_H
+#define MOE_EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- limits ------------------------------------------------------------ */
+#define MOE_MAX_EXPERTS 1024   /* E */
+#define MOE_MAX_TOPK 32        /* k */
+#define MOE_MAX_RANKS 1024     /* P */
+
+/* ---- dtypes ------------------------------------------------------------ */
+#define MOE_BF16 0
+#define MOE_FP8_E4M3 1
+
+/* ---- return codes -------------------------------------------------------- */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)  /* null pointer, negative size, E % P != 0, k > E ... */
+#define MOE_ERR_UNSUPPORTED (-2)  /* a size beyond the MOE_MAX_* limits, H % 8, FP8 with H % 128 */
+#define MOE_ERR_WORKSPACE (-3)    /* workspace too small or not 256-byte aligned */
+#define MOE_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed */
+#define MOE_ERR_STATE (-5)        /* call order violated (combine before dispatch ...) */
+
+/* ---- device status bits (sticky until moe_read_status clears them) ------ */
+#define MOE_STATUS_BAD_EXPERT_ID 0x1u  /* an id outside [-1, E): slot treated as masked */
+#define MOE_STATUS_TIMEOUT 0x2u        /* a bounded device wait gave up */
+
+/* Problem description. Passed by pointer; copied into the handle. */
+typedef struct {
+    int32_t num_ranks;       /* P >= 1 virtual EP ranks */
+    int32_t tokens_per_rank; /* T_r >= 1 */
+    int32_t num_experts;     /* E, a multiple of P, <= MOE_MAX_EXPERTS */
+    int32_t top_k;           /* k, 1 <= k <= min(E, MOE_MAX_TOPK) */
+    int32_t hidden;          /* H, a multiple of 8; a multiple of 128 for FP8 */
+    int32_t dispatch_dtype;  /* MOE_BF16 or MOE_FP8_E4M3 (per-128-channel fp32 scales) */
+    int32_t combine_dtype;   /* MOE_BF16 (the only combine dtype) */
+    int32_t expert_capacity; /* per-expert row limit c; 0 = unlimited ([A2A] 8.1) */
+} moe_config_t;
+
+/* Opaque handle: configuration + pointers into the caller's workspace. */
+typedef struct moe_handle *moe_handle_t;
+
+/* Device pointers to the layout inside the workspace, valid after
+ * moe_dispatch_layout (counts/offsets) and moe_dispatch (inv). All int32.
+ *   expert_count[E]       n_e: receive rows of expert e after capacity
+ *   expert_count_raw[E]   valid assignments to e before capacity
+ *   expert_offset[E+1]    first receive row of expert e; [E] = total rows.
+ *                         Experts are contiguous and in global order, so the
+ *                         rows of rank d are [rank_base[d], rank_base[d+1]).
+ *   src_expert_count[P*E] cnt[s][e]: valid assignments from source s to e
+ *   src_expert_kept[P*E]  the same after capacity
+ *   count_matrix[P*P]     C[s][d]: kept assignments from source s to rank d
+ *                         ([EP] "All-to-All-v")
+ *   send_offset[P*P]      exclusive prefix of C[s][.] over d ([EP] prefix sum)
+ *   recv_offset[P*E]      first receive row of source s inside expert e
+ *   rank_base[P+1]        first receive row of rank d; [P] = total rows
+ *   inv[T*k]              receive row of assignment a, -1 if masked/dropped
+ *                         (written by moe_dispatch)
+ *   totals[4]             kept rows, dropped (capacity), masked (id -1 or bad),
+ *                         reserved
+ * Contents are overwritten by the next layout call on the handle. */
+typedef struct {
+    int32_t *expert_count;
+    int32_t *expert_count_raw;
+    int32_t *expert_offset;
+    int32_t *src_expert_count;
+    int32_t *src_expert_kept;
+    int32_t *count_matrix;
+    int32_t *send_offset;
+    int32_t *recv_offset;
+    int32_t *rank_base;
+    int32_t *inv;
+    int32_t *totals;
+} moe_layout_view_t;
+
+/* Per-receive-row metadata ([EP] payload schema: local expert id, source
+ * token index, top-k slot / routing weight; the source rank travels with it so
+ * combine can route the row home). Each array has rows_max entries (see
+ * moe_recv_rows_max); rows at or beyond the total kept count are untouched. */
+typedef struct {
+    int32_t *local_expert; /* e mod L */
+    int32_t *src_rank;     /* s */
+    int32_t *src_token;    /* t, local to the source rank */
+    int32_t *slot;         /* j */
+    float *weight;         /* w[g, j] */
+} moe_recv_meta_t;
+
+/* Bytes of device workspace a handle for *cfg needs (0 if *cfg is invalid). */
+size_t moe_workspace_bytes(const moe_config_t *cfg);
+
+/* Receive rows every recv_* buffer must hold: T*k, or E*c when a capacity c is
+ * set and smaller ([EP] "Memory is not only expert weights": preallocate by
+ * the worst case). 0 if *cfg is invalid. */
+int64_t moe_recv_rows_max(const moe_config_t *cfg);
+
+/* Creates a handle over d_workspace (device, >= moe_workspace_bytes(cfg)
+ * bytes, 256-byte aligned, owned by the caller and not freed by the library).
+ * Zeroes the workspace's control words with a synchronous cudaMemset on the
+ * current device; call once at set-up, outside stream capture.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+int moe_handle_create(const moe_config_t *cfg, void *d_workspace, size_t bytes,
+                      moe_handle_t *out);
+
+/* Frees the host-side handle only. NULL is accepted. */
+int moe_handle_destroy(moe_handle_t h);
+
+/* a1 -- router top-k ([PPLX] introduction; [EP] router output [T, k]).
+ * logits: fp32 [T, E]. Writes ids int32 [T, k] (slot 0 = largest logit; equal
+ * logits ordered by the lower expert index) and w fp32 [T, k] = softmax over
+ * the k chosen logits (= full softmax renormalised over them), evaluated in
+ * double and rounded to fp32. Logits must be finite. */
+int moe_route_topk(moe_handle_t h, const float *logits, int32_t *ids, float *w,
+                   void *stream);
+
+/* a2..a3 -- count + prefix scan + capacity from given ids ([EP] "Why count
+ * and permute before dispatch", "All-to-All-v"; [A2A] 3.5, 8.1).
+ * ids: int32 [T, k]; -1 marks a padded/invalid slot. Computes every array of
+ * moe_layout_view_t except inv. The receive order is the stable order
+ * (expert, source rank, token, slot); with a capacity c, the first c
+ * assignments of each expert in that order are kept. */
+int moe_dispatch_layout(moe_handle_t h, const int32_t *ids, void *stream);
+
+/* a1 + a2..a3 fused in one kernel: routes logits (as moe_route_topk, writing
+ * ids and w) and builds the layout from the routed ids. */
+int moe_route_dispatch_layout(moe_handle_t h, const float *logits, int32_t *ids,
+                              float *w, void *stream);
+
+/* Layout pointers (device) of the handle's workspace. Host-only, no launch. */
+int moe_get_layout(moe_handle_t h, moe_layout_view_t *out);
+
+/* a4..a5 -- permute + pack + all-to-all-v scatter ([A2A] 4.3, 5.2; [EP]
+ * payload schema, bijection). Needs a preceding layout call on the handle.
+ * x: bf16 [T, H]; w: fp32 [T, k] (the weights that travel with the rows).
+ * recv_x: rows_max rows of H elements: bf16 for MOE_BF16, e4m3 bytes for
+ * MOE_FP8_E4M3. recv_scale: fp32 [rows_max, H/128] for FP8 (per token and
+ * 128-channel block: s = amax/448 in fp32, codes = e4m3 RNE satfinite of
+ * x/s; an all-zero block has s = 0 and zero codes), NULL for BF16.
+ * meta: per-row metadata arrays. Also writes the layout's inv[T*k]. */
+int moe_dispatch(moe_handle_t h, const void *x, const float *w, void *recv_x,
+                 float *recv_scale, const moe_recv_meta_t *meta, void *stream);
+
+/* a6 -- expert stand-in (the pages' grouped GEMM is out of scope): for every
+ * kept receive row r of expert e, y[r] = bf16(c[e] * x_r), where x_r is the
+ * bf16 payload (c = NULL means c[e] = 1) or, for FP8, the dequantised value
+ * e4m3(q) * s. y: bf16 [rows_max, H]. Needs a preceding moe_dispatch with the
+ * same recv_x / recv_scale. */
+int moe_expert_standin(moe_handle_t h, const void *recv_x, const float *recv_scale,
+                       const float *expert_scale, void *y, void *stream);
+
+/* a7 -- combine + unpermute ([EP] "Combine is not simply sending results
+ * back"; [PPLX] "Combine"): out[g] = bf16_rne(acc), acc = 0.0f and, for
+ * j = 0..k-1 in slot order with inv[g*k+j] >= 0,
+ * acc = fmaf(w[g,j], y[inv[g*k+j]], acc). Masked and dropped slots add
+ * nothing; weights are not renormalised. y: bf16 [rows_max, H] in receive
+ * order; w: fp32 [T, k]; out: bf16 [T, H]. Needs a preceding moe_dispatch. */
+int moe_combine(moe_handle_t h, const void *y, const float *w, void *out,
+                void *stream);
+
+/* Reads and clears the device status word. Synchronises `stream`: tests and
+ * debugging only. *flags receives MOE_STATUS_* bits. */
+int moe_read_status(moe_handle_t h, uint32_t *flags, void *stream);
+
+/* Human-readable name of a MOE_ERR_* code (static string). */
+const char *moe_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_EP_H */
