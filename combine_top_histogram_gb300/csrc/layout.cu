@@ -369,14 +369,24 @@ size_t layout_smem_bytes(int E, int tpc, int k) {
   return sizeof(int) * ((size_t)(wcnt_ints > scan_ints ? wcnt_ints : scan_ints) + (size_t)tpc * k);
 }
 
+// The dynamic shared-memory limit is a per-kernel setting shared by every
+// handle in the process, so it is raised to the device's opt-in maximum (never
+// lowered to one configuration's need); the launch itself asks for what the
+// configuration uses.
 cudaError_t layout_prepare(int E, int tpc, int k) {
   const size_t smem = layout_smem_bytes(E, tpc, k);
+  int dev = 0, optin = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  if (smem > (size_t)optin) return cudaErrorInvalidValue;
   const int epl = experts_per_lane(E);
-  cudaError_t err = cudaFuncSetAttribute(layout_kernel_ptr<true>(epl),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  err = cudaFuncSetAttribute(layout_kernel_ptr<true>(epl),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   if (err != cudaSuccess) return err;
   return cudaFuncSetAttribute(layout_kernel_ptr<false>(epl),
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
 cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cudaStream_t st) {
