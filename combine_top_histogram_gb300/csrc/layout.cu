@@ -380,13 +380,17 @@ cudaError_t layout_prepare(int E, int tpc, int k) {
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (err != cudaSuccess) return err;
-  if (smem > (size_t)optin) return cudaErrorInvalidValue;
   const int epl = experts_per_lane(E);
-  err = cudaFuncSetAttribute(layout_kernel_ptr<true>(epl),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-  if (err != cudaSuccess) return err;
-  return cudaFuncSetAttribute(layout_kernel_ptr<false>(epl),
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  for (void* fn : {layout_kernel_ptr<true>(epl), layout_kernel_ptr<false>(epl)}) {
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, fn);
+    if (err != cudaSuccess) return err;
+    const int dyn_max = optin - (int)fa.sharedSizeBytes;  // static shared memory counts too
+    if (smem > (size_t)dyn_max) return cudaErrorInvalidValue;
+    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cudaStream_t st) {
