@@ -30,6 +30,7 @@ EXPORTED_SYMBOLS = (
     "moe_workspace_bytes", "moe_recv_rows_max", "moe_handle_create", "moe_handle_destroy",
     "moe_route_topk", "moe_dispatch_layout", "moe_route_dispatch_layout", "moe_get_layout",
     "moe_dispatch", "moe_expert_standin", "moe_combine", "moe_read_status", "moe_error_string",
+    "moe_dispatch_layout_noalloc",
 )
 
 
@@ -103,6 +104,8 @@ def load_library():
         lib.moe_combine.argtypes = [vp, vp, vp, vp, vp]
         lib.moe_read_status.restype = i32
         lib.moe_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
+        lib.moe_dispatch_layout_noalloc.restype = i32
+        lib.moe_dispatch_layout_noalloc.argtypes = [cfgp, vp, ctypes.POINTER(moe_layout_view_t), vp]
         lib.moe_error_string.restype = ctypes.c_char_p
         lib.moe_error_string.argtypes = [i32]
         _lib = lib
@@ -247,6 +250,17 @@ def moe_read_status(h: Handle, stream=None) -> int:
     _check("moe_read_status", load_library().moe_read_status(
         h.ptr, ctypes.byref(flags), _stream(stream)))
     return int(flags.value)
+
+
+def moe_dispatch_layout_noalloc(cfg: moe_config_t, ids, out: dict, stream=None) -> None:
+    """Layout + inverse permutation into caller tensors (int32, sized as in
+    moe_get_layout's views), with no device allocation by the library. For
+    callers that cannot allocate (graph capture, fixed-pool runtimes); the
+    first call on a device must precede any stream capture; overlapping calls
+    race on the library's static scratch."""
+    v = moe_layout_view_t(*(_ptr(out[n]) for n, _ in moe_layout_view_t._fields_))
+    _check("moe_dispatch_layout_noalloc", load_library().moe_dispatch_layout_noalloc(
+        ctypes.byref(cfg), _ptr(ids), ctypes.byref(v), _stream(stream)))
 
 
 def moe_error_string(code: int) -> str:

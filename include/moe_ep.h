@@ -207,6 +207,32 @@ int moe_expert_standin(moe_handle_t h, const void *recv_x, const float *recv_sca
 int moe_combine(moe_handle_t h, const void *y, const float *w, void *out,
                 void *stream);
 
+/* ---- layout without any device allocation -------------------------------
+ * The pages have no counterpart for this entry point. It serves callers that
+ * may not allocate device memory and have no workspace to hand over: code
+ * running while a CUDA graph is being captured, host frameworks whose plugin
+ * interface passes only inputs and outputs, processes whose device allocator
+ * belongs to someone else. It computes what moe_dispatch_layout computes plus
+ * the inverse permutation inv[T*k] (which the workspace path writes during
+ * moe_dispatch), from ids int32 [T, k], into the caller's arrays named by
+ * *out (every pointer of moe_layout_view_t must be a device array of the size
+ * given there). No cudaMalloc, cudaFree or allocating library routine is
+ * called. Intermediate data lives in one file-scope device array of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
+ * until the process exits; a problem whose scratch (256 + 4*E*P*ceil(T_r/c)
+ * + 4*T*k bytes, each term rounded up to 256, c = chunk tokens) exceeds it
+ * returns MOE_ERR_UNSUPPORTED and enqueues nothing.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. Every call shares the array and finds the previous call's
+ * contents: each call clears the control words first, and calls that overlap
+ * on the GPU (other streams, other threads) race and must be serialised by
+ * the caller. Ids outside [-1, E) are counted as masked; there is no status
+ * word. Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int moe_dispatch_layout_noalloc(const moe_config_t *cfg, const int32_t *ids,
+                                const moe_layout_view_t *out, void *stream);
+
 /* Reads and clears the device status word. Synchronises `stream`: tests and
  * debugging only. *flags receives MOE_STATUS_* bits. */
 int moe_read_status(moe_handle_t h, uint32_t *flags, void *stream);
