@@ -5,8 +5,9 @@ One step = one MoE layer's hot path over one batch of synthetic tokens:
 (route +) count + scan (one fused kernel) -> dispatch pack/scatter -> [expert
 stand-in, untimed] -> combine. The timed value is the device time of the
 layout + dispatch + combine kernels (CUDA events on the launching stream), with
-L2 flushed (a 320 MB write) before the dispatch phase and again before the
-combine phase of every step, so every phase starts cold.
+L2 flushed (a 320 MB write, then a 320 MB read so that no dirty line of the
+flush is written back inside a timed kernel) before the dispatch phase and
+again before the combine phase of every step, so every phase starts cold.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|...]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
@@ -267,7 +268,15 @@ def run_ours(args, wl, rank, world, local):
         ids = torch.from_numpy(inp.ids).to(dev)
         w = torch.from_numpy(inp.w).to(dev)
     c = torch.from_numpy(inp.expert_scale).to(dev) if inp.expert_scale is not None else None
-    flush_buf = torch.empty(320 << 20, dtype=torch.uint8, device=dev)
+    # L2 flush: write 320 MB (evicts everything), then read another 320 MB so
+    # the dirty lines of the write are written back here, outside the timed
+    # region, and the next phase starts with a cold, clean L2.
+    flush_w = torch.empty(320 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(80 << 20, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.sum()
 
     def layout():
         if routed:
@@ -277,7 +286,7 @@ def run_ours(args, wl, rank, world, local):
 
     def step(ev, flush_before_combine=True, flush_before=True):
         if flush_before:
-            flush_buf.zero_()
+            flush_l2()
         ev[0].record(stream)
         layout()
         ev[1].record(stream)
@@ -285,7 +294,7 @@ def run_ours(args, wl, rank, world, local):
         ev[2].record(stream)
         layer.expert(c, stream)
         if flush_before_combine:
-            flush_buf.zero_()
+            flush_l2()
         ev[3].record(stream)
         layer.combine(w, stream)
         ev[4].record(stream)
@@ -335,7 +344,7 @@ def run_ours(args, wl, rank, world, local):
     e2e_ms = []
     eevs = new_events(min(args.steps, 50) + 3)
     for i, ev in enumerate(eevs):
-        flush_buf.zero_()
+        flush_l2()
         ev[0].record(stream)
         x.copy_(x_h, non_blocking=True)
         for a, b in zip(r_d, r_h):
@@ -344,7 +353,7 @@ def run_ours(args, wl, rank, world, local):
         layer.dispatch(x, w, stream)
         ev[1].record(stream)
         layer.expert(c, stream)
-        flush_buf.zero_()
+        flush_l2()
         ev[2].record(stream)
         layer.combine(w, stream)
         out_h.copy_(layer.out, non_blocking=True)
@@ -380,8 +389,8 @@ def run_ours(args, wl, rank, world, local):
         "dtype": "fp8_e4m3+bf16" if layer.fp8 else "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "P": wl.P, "tokens_per_rank": wl.Tr, "E": wl.E,
                    "top_k": wl.k, "hidden": wl.H, "capacity": wl.cap,
-                   "l2": "flushed (320 MB write) before the dispatch and the combine phase "
-                         "of every timed step",
+                   "l2": "flushed (320 MB write, then 320 MB read) before the dispatch and "
+                         "the combine phase of every timed step",
                    "replicas": world},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

@@ -32,6 +32,10 @@ int validate(const moe_config_t* c) {
   if (c->dispatch_dtype == MOE_FP8_E4M3 && c->hidden % 128 != 0) return MOE_ERR_UNSUPPORTED;
   const long long T = (long long)c->num_ranks * c->tokens_per_rank;
   if (T * c->top_k >= (1ll << 31) - 1) return MOE_ERR_UNSUPPORTED;  // int32 row indices
+  // The layout kernel keeps its per-(source, expert) tables in shared memory.
+  if (moe::layout_smem_bytes(c->num_experts, moe::kMaxChunkAssign / c->top_k, c->top_k,
+                             c->num_ranks) > moe::kLayoutSmemLimit)
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -44,8 +48,8 @@ struct Plan {
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 // Chunking of the layout kernel. Given ids, a chunk of ~2048 assignments
-// keeps the scan short; when routing, chunks are cut smaller so the top-k
-// work (one warp per token) spreads over about two CTAs per SM.
+// keeps the scan short; when routing, chunks are cut smaller (down to one
+// token group per warp) so the top-k work spreads over about two CTAs per SM.
 Plan make_plan(const moe_config_t* c, int num_sms) {
   Plan p{};
   const int P = c->num_ranks, Tr = c->tokens_per_rank, E = c->num_experts, k = c->top_k;
@@ -57,8 +61,11 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   if (tpc > Tr) tpc = Tr;
   p.tpc_ids = tpc;
   p.cps_ids = ceil_div(Tr, tpc);
+  int k2 = 1;
+  while (k2 < k) k2 <<= 1;
+  const int group = 32 / k2;  // tokens one warp routes together
   int tr = (int)((T + 2ll * num_sms - 1) / (2ll * num_sms));
-  if (tr < moe::kLayoutWarps) tr = moe::kLayoutWarps;
+  if (tr < moe::kLayoutWarps * group) tr = moe::kLayoutWarps * group;
   if (tr > 2048 / k) tr = 2048 / k;
   if (tr < 1) tr = 1;
   if (tr > max_tpc) tr = max_tpc;
@@ -165,7 +172,7 @@ int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
   if (bytes < p.bytes || !aligned(d_workspace, kAlign)) return MOE_ERR_WORKSPACE;
   // Opt in to the layout kernel's shared memory for the larger chunking.
   const int tpc_max = p.tpc_route > p.tpc_ids ? p.tpc_route : p.tpc_ids;
-  if (moe::layout_prepare(cfg->num_experts, tpc_max, cfg->top_k) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::layout_prepare(cfg->num_experts, tpc_max, cfg->top_k, cfg->num_ranks) != cudaSuccess) return MOE_ERR_CUDA;
 
   moe_handle* h = static_cast<moe_handle*>(calloc(1, sizeof(moe_handle)));
   if (!h) return MOE_ERR_INVALID_ARG;

@@ -122,7 +122,6 @@ cudaError_t launch_combine_k(const CombineArgs& a, int blocks, cudaStream_t st) 
 // Expert stand-in: one CTA per receive row; the row's global expert is found
 // by binary search in expert_offset.
 __global__ void __launch_bounds__(128) k_standin(const StandinArgs p) {
-  __shared__ int e_s;
   __shared__ float c_s;
   const int nvec = p.H >> 3;
   const int total = __ldg(p.expert_offset + p.E);
@@ -134,7 +133,6 @@ __global__ void __launch_bounds__(128) k_standin(const StandinArgs p) {
         if (__ldg(p.expert_offset + mid) <= r) lo = mid;
         else hi = mid - 1;
       }
-      e_s = lo;
       c_s = p.expert_scale ? __ldg(p.expert_scale + lo) : 1.0f;
     }
     __syncthreads();

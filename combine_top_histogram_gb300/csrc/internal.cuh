@@ -16,6 +16,11 @@ constexpr int kLayoutWarps = kLayoutThreads / 32;
 // Assignments per layout chunk are bounded so that a chunk-local rank fits in
 // the low 16 bits of an assignment code (code = expert << 16 | rank).
 constexpr int kMaxChunkAssign = 4096;
+// The device-wide scan stages the chunk table through shared memory in tiles
+// of this many int32 (16 per thread); E must not exceed it.
+constexpr int kScanTile = kLayoutThreads * 16;
+// Shared memory the layout kernel may use per CTA (GB300: 227 KB opt-in).
+constexpr size_t kLayoutSmemLimit = 220 * 1024;
 
 // Per-assignment code written by the layout kernel and read by dispatch:
 // (expert << 16) | (stable rank of the assignment among the chunk's
@@ -89,8 +94,8 @@ struct StandinArgs {
 cudaError_t launch_layout(const LayoutArgs& a, bool route, int num_sms, cudaStream_t st);
 cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long long T,
                               int E, int k, int num_sms, cudaStream_t st);
-size_t layout_smem_bytes(int E, int tpc, int k);
-cudaError_t layout_prepare(int E, int tpc, int k);
+size_t layout_smem_bytes(int E, int tpc, int k, int P);
+cudaError_t layout_prepare(int E, int tpc, int k, int P);
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_standin(const StandinArgs& a, int num_sms, cudaStream_t st);

@@ -13,15 +13,19 @@
 // Design (one GPU, P virtual ranks in one HBM):
 //   * The assignment list (s, t, j) is cut into chunks of whole tokens that
 //     never straddle a source rank. One CTA per chunk.
-//   * Route mode: each warp takes one token, holds its E logits in registers
-//     (E/32 per lane), and picks the top-k by k warp-wide arg-max reductions
-//     (value descending, expert ascending on ties).
-//   * Every warp owns a contiguous sub-range of the chunk. Pass 1 counts its
-//     experts with __match_any_sync (one shared-memory add per distinct expert
-//     per 32 assignments); a per-expert scan over the 16 warps gives each warp
-//     its base; pass 2 re-walks the sub-range and gives each assignment its
-//     stable rank = warp base + lanes of the same expert below it. No atomics
-//     decide any position, so the layout is deterministic.
+//   * Route mode: a warp routes 32/k tokens (k rounded up to a power of
+//     two): for each it holds the E logits as order-preserving keys in
+//     registers (E/32 per lane) and picks the top-k by k rounds of a warp
+//     max-reduction plus a min-reduction over tied expert indices (value
+//     descending, expert ascending on ties); then all their softmax weights
+//     are evaluated at once, one lane per (token, slot).
+//   * Every warp owns a contiguous sub-range of the chunk. Pass 1 finds, for
+//     every 32 assignments, the lanes sharing an expert (one ballot per bit of
+//     the expert id) and adds their count once per distinct expert; a
+//     per-expert scan over the 16 warps gives each warp its base; pass 2
+//     re-walks the sub-range and gives each assignment its stable rank = warp
+//     base + lanes of the same expert below it. No atomics decide any
+//     position, so the layout is deterministic.
 //   * The chunk histogram goes to global memory; the last CTA to arrive
 //     (threadfence + arrival counter, no spinning) scans all chunk histograms
 //     and derives n_e, expert_offset, cnt[s][e], C[s][d], send_offset,
@@ -30,12 +34,26 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "ffmath.cuh"
 #include "internal.cuh"
 
 namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+
+// Lanes of the warp holding the same expert id as this lane (valid ids >= 0),
+// from one ballot per bit of the id: the bit-plane form of a warp multisplit
+// (Ashkiani et al., "GPU Multisplit", PPoPP 2016). Undefined for e < 0.
+__device__ __forceinline__ unsigned peer_mask(int e, int nbits) {
+  unsigned m = __ballot_sync(kFull, e >= 0);
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned bb = __ballot_sync(kFull, bit);
+    m &= bit ? bb : ~bb;
+  }
+  return m;
+}
 
 // Exclusive scan in place of a[0..n) held in shared memory, by the whole CTA.
 // tmp: 32 ints of shared scratch. Returns the total. Ends with __syncthreads.
@@ -76,154 +94,225 @@ __device__ int cta_exclusive_scan(int* a, int n, int* tmp) {
   return total;
 }
 
-// Top-k of one token's logits by one warp. Lane j < k returns slot j's expert
-// id and its double-precision softmax weight over the chosen logits.
-// Expert index of register i of a lane is i*32 + lane (coalesced loads).
+// Order-preserving map of a finite float to an unsigned key (larger float ->
+// larger key); -0 is mapped like +0 so that equal logits tie. Key 0 is below
+// every finite float and marks an empty or already chosen register.
+__device__ __forceinline__ unsigned order_key(float v) {
+  const unsigned u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of one token by one warp: k rounds of a warp-wide arg-max (larger
+// logit first, lower expert index on ties), each round one max-reduction of
+// the keys and one min-reduction of the tied candidates' expert indices.
+// Register i of a lane holds expert i*32 + lane. Lane j < k returns slot j.
 template <int EPL>
-__device__ void route_token_warp(const float* __restrict__ z, int E, int k, int lane,
-                                 int& out_id, float& out_w) {
-  float v[EPL];
+__device__ __forceinline__ void topk_select(const float* __restrict__ z, int E, int k, int lane,
+                                            int& out_id, float& out_z) {
+  unsigned key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = i * 32 + lane;
-    v[i] = e < E ? __ldg(z + e) : -INFINITY;
+    key[i] = e < E ? order_key(__ldg(z + e)) : 0u;
   }
-  unsigned taken = 0;  // bit i: register i already chosen
-  int my_id = -1;
-  float my_z = 0.f;
+  out_id = -1;
+  out_z = 0.0f;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    unsigned bk = 0u;
+    unsigned bi = 0xffffffffu;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      const int e = i * 32 + lane;
-      if (e < E && !((taken >> i) & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
-        bv = v[i];
-        bi = e;
+      if (key[i] > bk) {  // strict: the lowest register (expert) wins a tie in a lane
+        bk = key[i];
+        bi = (unsigned)(i * 32 + lane);
       }
     }
+    const unsigned m = __reduce_max_sync(kFull, bk);
+    const unsigned win = __reduce_min_sync(kFull, bk == m ? bi : 0xffffffffu);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, bv, o);
-      const int oi = __shfl_xor_sync(kFull, bi, o);
-      // total order: larger value first, then smaller expert index; an empty
-      // candidate (index INT_MAX) loses to any real one.
-      const bool take = (oi != 0x7fffffff) &&
-                        (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-      if (take) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    for (int i = 0; i < EPL; ++i)
+      if (win == (unsigned)(i * 32 + lane)) key[i] = 0u;
     if (lane == j) {
-      my_id = bi;
-      my_z = bv;
+      out_id = (int)win;
+      out_z = key_value(m);
     }
   }
-  // Softmax over the chosen logits, in double, summed in slot order.
-  const double z0 = (double)__shfl_sync(kFull, my_z, 0);
-  const double ex = lane < k ? exp((double)my_z - z0) : 0.0;
-  double sum = 0.0;
-  for (int j = 0; j < k; ++j) sum += __shfl_sync(kFull, ex, j);
-  out_id = my_id;
-  out_w = (float)(ex / sum);
 }
 
-__device__ void layout_scan(const LayoutArgs& p, int* smem) {
-  const int E = p.E, P = p.P, NT = blockDim.x, tid = threadIdx.x;
-  int ng = NT / E;
-  if (ng < 1) ng = 1;
-  if (ng > p.nchunks) ng = p.nchunks;
-  const int seg = (p.nchunks + ng - 1) / ng;
-  int* part = smem;                          // [ng*E] <= max(NT, E)
-  int* sk = part + (NT > E ? NT : E);        // [E]  n_kept -> expert_offset
-  int* sraw = sk + E;                        // [E]
-  int* tmp = sraw + E;                       // [32]
-  int* red = tmp + 32;                       // [2]
+__device__ __forceinline__ float pow2f(int n) {  // 2^n for -126 <= n <= 127
+  return __uint_as_float((unsigned)(n + 127) << 23);
+}
 
-  // (1) per-expert column scan over chunks, two levels: segment sums ...
-  for (int it = tid; it < ng * E; it += NT) {
-    const int e = it % E, gi = it / E;
-    const int b0 = gi * seg, b1 = min(p.nchunks, b0 + seg);
-    int sum = 0;
-    for (int b = b0; b < b1; ++b) sum += __ldcg(p.hist + (long long)b * E + e);
-    part[gi * E + e] = sum;
+// Routes up to G = 32/K2 consecutive tokens with one warp (K2 = k rounded up
+// to a power of two): selects each token's top-k, then evaluates all their
+// softmax weights at once, token t's slot j on lane t*K2 + j. Weights are
+// w_j = exp(z_j - z_0) / sum_i exp(z_i - z_0) in float-float arithmetic (see
+// ffmath.cuh), rounded once to fp32; the sum is a butterfly inside the lane
+// group (its order does not matter at this precision).
+// Returns, per lane, its token (lane / K2), slot (lane % K2), id and weight;
+// valid is false for lanes past the token count or the top-k.
+template <int EPL>
+__device__ __forceinline__ void route_group_warp(const float* __restrict__ logits, long long g0,
+                                                 int ntok, int E, int k, int K2, int lane,
+                                                 bool& valid, int& id, float& w) {
+  const int grp = lane / K2, slot = lane - grp * K2;
+  valid = grp < ntok && slot < k;
+  id = -1;
+  float my_z = 0.0f;
+  for (int t = 0; t < ntok; ++t) {
+    int tid_;
+    float tz;
+    topk_select<EPL>(logits + (g0 + t) * (long long)E, E, k, lane, tid_, tz);
+    const int src = slot < 32 ? slot : 0;
+    const int sid = __shfl_sync(kFull, tid_, src);
+    const float sz = __shfl_sync(kFull, tz, src);
+    if (grp == t) {
+      id = sid;
+      my_z = sz;
+    }
   }
+  const float z0 = __shfl_sync(kFull, my_z, lane & ~(K2 - 1));
+  const ff::F2 d = valid ? ff::two_sum(my_z, -z0) : ff::F2{0.0f, 0.0f};  // exact, <= 0
+  const bool tiny = d.hi < -80.0f;  // exp(d) < 2^-115: evaluated separately below
+  int n = 0;
+  const ff::F2 m = ff::exp_reduced(tiny ? ff::F2{0.0f, 0.0f} : d, n);
+  const float sc = pow2f(n);
+  ff::F2 sum = (valid && !tiny) ? ff::F2{__fmul_rn(m.hi, sc), __fmul_rn(m.lo, sc)}
+                                : ff::F2{0.0f, 0.0f};
+  for (int o = K2 >> 1; o > 0; o >>= 1) {
+    const ff::F2 other{__shfl_xor_sync(kFull, sum.hi, o), __shfl_xor_sync(kFull, sum.lo, o)};
+    sum = ff::add(sum, other);
+  }
+  if (!tiny) {
+    const ff::F2 q = ff::div(m, sum);
+    w = __fmul_rn(__fadd_rn(q.hi, q.lo), sc);
+  } else {
+    // logit gap above 80 inside the top-k: a weight below 2^-115, in double
+    w = (float)(exp((double)my_z - (double)z0) / ((double)sum.hi + (double)sum.lo));
+  }
+}
+
+// Device-wide scan by the last chunk CTA. The chunk table [nchunks][E] is
+// staged through shared memory in tiles of kScanTile ints (coalesced loads, the
+// next tile's loads in flight while the current one is scanned); each thread
+// owns expert columns and carries the running count across tiles. The
+// per-(source, expert) prefixes at source boundaries, the kept counts and the
+// count matrix stay in shared memory, so no step walks global memory serially.
+__device__ void layout_scan(const LayoutArgs& p, int* tile, int* rest) {
+  const int E = p.E, P = p.P, tid = threadIdx.x;
+  constexpr int NT = kLayoutThreads;
+  constexpr int PER = kScanTile / NT;  // staged values per thread per tile
+  int* run = rest;                  // [E]        running column sums
+  int* pre = run + E;               // [(P+1)*E]  prefix at each source's first chunk
+  int* sk = pre + (P + 1) * E;      // [E]        kept counts -> expert offsets
+  int* Cs = sk + E;                 // [P*P]      count matrix
+  int* tmp = Cs + P * P;            // [32]
+  int* red = tmp + 32;              // [2]        dropped, raw total
+
+  const int TB = kScanTile / E;     // chunks per tile (E <= kScanTile)
+  for (int e = tid; e < E; e += NT) run[e] = 0;
   if (tid < 2) red[tid] = 0;
-  __syncthreads();
-  // ... exclusive over segments, totals per expert, capacity clamp ...
-  for (int e = tid; e < E; e += NT) {
-    int run = 0;
-    for (int gi = 0; gi < ng; ++gi) {
-      const int v = part[gi * E + e];
-      part[gi * E + e] = run;
-      run += v;
+
+  int stage[PER];
+  auto load_tile = [&](int b0) {
+    const int n = min(TB, p.nchunks - b0) * E;
+    const int* src = p.hist + (long long)b0 * E;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = q * NT + tid;
+      stage[q] = i < n ? __ldcg(src + i) : 0;
     }
-    const int kept = (p.cap > 0 && run > p.cap) ? p.cap : run;
-    sraw[e] = run;
-    sk[e] = kept;
-    p.n_raw[e] = run;
-    p.n_kept[e] = kept;
+  };
+  load_tile(0);
+  for (int b0 = 0; b0 < p.nchunks; b0 += TB) {
+    const int nb = min(TB, p.nchunks - b0);
+    const int n = nb * E;
+    __syncthreads();  // previous tile fully stored / run[] initialised
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int i = q * NT + tid;
+      if (i < n) tile[i] = stage[q];
+    }
+    __syncthreads();
+    if (b0 + TB < p.nchunks) load_tile(b0 + TB);  // consumed next iteration
+    const int s_first = (b0 + p.cps - 1) / p.cps;  // first source starting in this tile
+    for (int e = tid; e < E; e += NT) {
+      int r = run[e];
+      int s_next = s_first, b_next = s_first * p.cps;
+      for (int bb = 0; bb < nb; ++bb) {
+        if (b0 + bb == b_next) {  // first chunk of source s_next
+          pre[s_next * E + e] = r;
+          ++s_next;
+          b_next += p.cps;
+        }
+        const int v = tile[bb * E + e];
+        tile[bb * E + e] = r;
+        r += v;
+      }
+      run[e] = r;
+    }
+    __syncthreads();
+    int* dst = p.hist + (long long)b0 * E;
+    for (int i = tid; i < n; i += NT) dst[i] = tile[i];
   }
   __syncthreads();
-  // ... and the exclusive chunk bases, in place.
-  for (int it = tid; it < ng * E; it += NT) {
-    const int e = it % E, gi = it / E;
-    const int b0 = gi * seg, b1 = min(p.nchunks, b0 + seg);
-    int run = part[gi * E + e];
-    for (int b = b0; b < b1; ++b) {
-      int* h = p.hist + (long long)b * E + e;
-      const int v = __ldcg(h);
-      *h = run;
-      run += v;
-    }
-  }
-  // (2) expert offsets: exclusive scan of kept counts over global expert order.
-  const int total = cta_exclusive_scan(sk, E, tmp);
-  for (int e = tid; e <= E; e += NT) p.expert_offset[e] = e < E ? sk[e] : total;
-  // (3) per (source, expert): raw and kept counts, receive offsets.
-  for (int it = tid; it < P * E; it += NT) {
-    const int s = it / E, e = it - s * E;
-    const int pre = __ldcg(p.hist + (long long)(s * p.cps) * E + e);
-    const int nxt = (s + 1 < P) ? __ldcg(p.hist + (long long)((s + 1) * p.cps) * E + e) : sraw[e];
-    const int c = nxt - pre;
-    int kept = c, start = pre;
-    if (p.cap > 0) {
-      kept = min(max(p.cap - pre, 0), c);
-      start = min(pre, p.cap);
-    }
-    p.cnt[it] = c;
-    p.kept_cnt[it] = kept;
-    p.recv_offset[it] = sk[e] + start;
-  }
-  // dropped and masked totals
+  // Per-expert totals, capacity clamp.
   {
     int dr = 0, rw = 0;
     for (int e = tid; e < E; e += NT) {
-      rw += sraw[e];
-      dr += sraw[e] - ((p.cap > 0 && sraw[e] > p.cap) ? p.cap : sraw[e]);
+      const int raw = run[e];
+      const int kept = (p.cap > 0 && raw > p.cap) ? p.cap : raw;
+      pre[P * E + e] = raw;
+      sk[e] = kept;
+      p.n_raw[e] = raw;
+      p.n_kept[e] = kept;
+      rw += raw;
+      dr += raw - kept;
     }
     if (dr) atomicAdd(&red[0], dr);
     if (rw) atomicAdd(&red[1], rw);
   }
   __syncthreads();
-  // (4) count matrix C[s][d] = kept assignments of s to experts owned by d.
+  // Expert offsets: exclusive scan of kept counts in global expert order.
+  const int total = cta_exclusive_scan(sk, E, tmp);
+  for (int e = tid; e <= E; e += NT) p.expert_offset[e] = e < E ? sk[e] : total;
+  // Per (source, expert): raw and kept counts, receive offsets.
+  for (int it = tid; it < P * E; it += NT) {
+    const int s = it / E, e = it - s * E;
+    const int a = pre[s * E + e];
+    const int c = pre[(s + 1) * E + e] - a;
+    int kept = c, start = a;
+    if (p.cap > 0) {
+      kept = min(max(p.cap - a, 0), c);
+      start = min(a, p.cap);
+    }
+    p.cnt[it] = c;
+    p.kept_cnt[it] = kept;
+    p.recv_offset[it] = sk[e] + start;
+  }
+  // Count matrix C[s][d]: kept assignments of source s to the experts of d.
   for (int it = tid; it < P * P; it += NT) {
     const int s = it / P, d = it - s * P;
     int sum = 0;
-    for (int e = d * p.L; e < (d + 1) * p.L; ++e) sum += __ldcg(p.kept_cnt + (long long)s * E + e);
+    for (int e = d * p.L; e < (d + 1) * p.L; ++e) {
+      const int a = pre[s * E + e];
+      const int c = pre[(s + 1) * E + e] - a;
+      sum += p.cap > 0 ? min(max(p.cap - a, 0), c) : c;
+    }
+    Cs[it] = sum;
     p.C[it] = sum;
   }
   for (int d = tid; d <= P; d += NT) p.rank_base[d] = d < P ? sk[d * p.L] : total;
   __syncthreads();
-  // (5) send offsets: exclusive prefix of C[s][.] over destinations.
+  // Send offsets: exclusive prefix of C[s][.] over destinations.
   for (int s = tid; s < P; s += NT) {
-    int run = 0;
+    int r = 0;
     for (int d = 0; d < P; ++d) {
-      const int v = __ldcg(p.C + (long long)s * P + d);
-      p.send_offset[(long long)s * P + d] = run;
-      run += v;
+      p.send_offset[(long long)s * P + d] = r;
+      r += Cs[s * P + d];
     }
   }
   if (tid == 0) {
@@ -240,10 +329,11 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
   extern __shared__ int smem[];
   __shared__ int s_last;
   const int E = p.E;
+  // Region A: per-warp expert counters, later the scan's staging tile.
+  // Region B: the chunk's expert ids, later the scan's tables.
   int* wcnt = smem;                                         // [warps][E]
   const int wcnt_ints = kLayoutWarps * E;
-  const int scan_ints = (kLayoutThreads > E ? kLayoutThreads : E) + 2 * E + 34;
-  int* ids_s = smem + (wcnt_ints > scan_ints ? wcnt_ints : scan_ints);  // [tpc*k]
+  int* ids_s = smem + (wcnt_ints > kScanTile ? wcnt_ints : kScanTile);  // [tpc*k]
 
   const int b = blockIdx.x;
   const int s = b / p.cps, c = b - s * p.cps;
@@ -257,14 +347,19 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
   for (int i = tid; i < wcnt_ints; i += kLayoutThreads) wcnt[i] = 0;
 
   if (ROUTE) {
-    for (int tl = warp; tl < nt; tl += kLayoutWarps) {
+    int K2 = 1;
+    while (K2 < p.k) K2 <<= 1;
+    const int G = 32 / K2;  // tokens routed together by one warp
+    for (int tl0 = warp * G; tl0 < nt; tl0 += kLayoutWarps * G) {
+      bool valid;
       int id;
       float wt;
-      route_token_warp<EPL>(p.logits + (g0 + tl) * (long long)E, E, p.k, lane, id, wt);
-      if (lane < p.k) {
-        ids_s[tl * p.k + lane] = id;
-        p.ids_out[(g0 + tl) * p.k + lane] = id;
-        p.w_out[(g0 + tl) * p.k + lane] = wt;
+      route_group_warp<EPL>(p.logits, g0 + tl0, min(G, nt - tl0), E, p.k, K2, lane, valid, id, wt);
+      if (valid) {
+        const int tl = tl0 + lane / K2, j = lane % K2;
+        ids_s[tl * p.k + j] = id;
+        p.ids_out[(g0 + tl) * p.k + j] = id;
+        p.w_out[(g0 + tl) * p.k + j] = wt;
       }
     }
   } else {
@@ -282,10 +377,12 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
   // Pass 1: per-warp expert counts of the warp's contiguous sub-range.
   const int per = (na + kLayoutWarps - 1) / kLayoutWarps;
   const int beg = min(na, warp * per), end = min(na, beg + per);
+  int nbits = 0;
+  while ((1 << nbits) < E) ++nbits;
   for (int base = beg; base < end; base += 32) {
     const int i = base + lane;
     const int e = i < end ? ids_s[i] : -1;
-    const unsigned m = __match_any_sync(kFull, e);
+    const unsigned m = peer_mask(e, nbits);
     if (e >= 0 && lane == __ffs(m) - 1) wcnt[warp * E + e] += __popc(m);
   }
   __syncthreads();
@@ -306,7 +403,7 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
   for (int base = beg; base < end; base += 32) {
     const int i = base + lane;
     const int e = i < end ? ids_s[i] : -1;
-    const unsigned m = __match_any_sync(kFull, e);
+    const unsigned m = peer_mask(e, nbits);
     int code = -1;
     if (e >= 0) code = (e << 16) | (wcnt[warp * E + e] + __popc(m & below));
     __syncwarp();
@@ -322,7 +419,7 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  layout_scan(p, smem);
+  layout_scan(p, smem, ids_s);
 }
 
 template <int EPL>
@@ -330,15 +427,21 @@ __global__ void __launch_bounds__(256) k_route_only(const float* __restrict__ lo
                                                     int32_t* ids, float* w, long long T, int E,
                                                     int k) {
   const int lane = threadIdx.x & 31;
+  int K2 = 1;
+  while (K2 < k) K2 <<= 1;
+  const int G = 32 / K2;
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long g = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < T;
-       g += warps) {
+  for (long long g0 = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * G; g0 < T;
+       g0 += warps * G) {
+    bool valid;
     int id;
     float wt;
-    route_token_warp<EPL>(logits + g * (long long)E, E, k, lane, id, wt);
-    if (lane < k) {
-      ids[g * k + lane] = id;
-      w[g * k + lane] = wt;
+    route_group_warp<EPL>(logits, g0, (int)min((long long)G, T - g0), E, k, K2, lane, valid, id,
+                          wt);
+    if (valid) {
+      const long long g = g0 + lane / K2;
+      ids[g * k + lane % K2] = id;
+      w[g * k + lane % K2] = wt;
     }
   }
 }
@@ -363,18 +466,19 @@ int experts_per_lane(int E) {
 
 }  // namespace
 
-size_t layout_smem_bytes(int E, int tpc, int k) {
-  const int wcnt_ints = kLayoutWarps * E;
-  const int scan_ints = (kLayoutThreads > E ? kLayoutThreads : E) + 2 * E + 34;
-  return sizeof(int) * ((size_t)(wcnt_ints > scan_ints ? wcnt_ints : scan_ints) + (size_t)tpc * k);
+size_t layout_smem_bytes(int E, int tpc, int k, int P) {
+  const size_t a = (size_t)(kLayoutWarps * E > kScanTile ? kLayoutWarps * E : kScanTile);
+  const size_t tables = (size_t)E + (size_t)(P + 1) * E + E + (size_t)P * P + 34;
+  const size_t ids = (size_t)tpc * k;
+  return sizeof(int) * (a + (tables > ids ? tables : ids));
 }
 
 // The dynamic shared-memory limit is a per-kernel setting shared by every
 // handle in the process, so it is raised to the device's opt-in maximum (never
 // lowered to one configuration's need); the launch itself asks for what the
 // configuration uses.
-cudaError_t layout_prepare(int E, int tpc, int k) {
-  const size_t smem = layout_smem_bytes(E, tpc, k);
+cudaError_t layout_prepare(int E, int tpc, int k, int P) {
+  const size_t smem = layout_smem_bytes(E, tpc, k, P);
   int dev = 0, optin = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -394,7 +498,7 @@ cudaError_t layout_prepare(int E, int tpc, int k) {
 }
 
 cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cudaStream_t st) {
-  const size_t smem = layout_smem_bytes(a.E, a.tpc, a.k);
+  const size_t smem = layout_smem_bytes(a.E, a.tpc, a.k, a.P);
   const int epl = experts_per_lane(a.E);
   void* fn = route ? layout_kernel_ptr<true>(epl) : layout_kernel_ptr<false>(epl);
   LayoutArgs args = a;

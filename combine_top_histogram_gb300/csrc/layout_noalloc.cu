@@ -108,7 +108,7 @@ extern "C" int moe_dispatch_layout_noalloc(const moe_config_t* cfg, const int32_
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   char* base = static_cast<char*>(scratch_address(dev));
   if (!base) return MOE_ERR_CUDA;
-  if (moe::layout_prepare(E, tpc, k) != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::layout_prepare(E, tpc, k, P) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The scratch keeps the previous call's contents: the control words (status
   // and the chunk arrival counter) must start at zero.

@@ -67,7 +67,9 @@ extern "C" {
 /* ---- return codes -------------------------------------------------------- */
 #define MOE_OK 0
 #define MOE_ERR_INVALID_ARG (-1)  /* null pointer, negative size, E % P != 0, k > E ... */
-#define MOE_ERR_UNSUPPORTED (-2)  /* a size beyond the MOE_MAX_* limits, H % 8, FP8 with H % 128 */
+#define MOE_ERR_UNSUPPORTED (-2)  /* a size beyond the MOE_MAX_* limits, H % 8, FP8 with H % 128,
+                                     or layout tables beyond shared memory: about
+                                     (P+1)*E + P*P + 2*E > 40000 int32 */
 #define MOE_ERR_WORKSPACE (-3)    /* workspace too small or not 256-byte aligned */
 #define MOE_ERR_CUDA (-4)         /* a CUDA runtime call or launch failed */
 #define MOE_ERR_STATE (-5)        /* call order violated (combine before dispatch ...) */

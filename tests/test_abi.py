@@ -42,7 +42,8 @@ def test_host_only_sizing_and_validation(cuda_lib):
     for bad in [B.make_config(3, 4, 8, 2, 64), B.make_config(2, 4, 8, 9, 64),
                 B.make_config(2, 4, 8, 2, 12), B.make_config(2, 4, 2048, 2, 64),
                 B.make_config(2, 4, 8, 2, 64, B.MOE_FP8_E4M3), B.make_config(0, 4, 8, 2, 64),
-                B.make_config(2, 4, 8, 2, 64, cap=-1), B.make_config(2, 4, 64, 33, 64)]:
+                B.make_config(2, 4, 8, 2, 64, cap=-1), B.make_config(2, 4, 64, 33, 64),
+                B.make_config(1024, 1, 1024, 1, 64), B.make_config(256, 2, 512, 2, 64)]:
         assert B.moe_workspace_bytes(bad) == 0
         assert B.moe_recv_rows_max(bad) == 0
         h = ctypes.c_void_p()
