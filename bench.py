@@ -2,9 +2,10 @@
 """Benchmark: MoE dispatch + combine, microseconds per layer, on one GB300.
 
 One step = one MoE layer's hot path over one batch of synthetic tokens:
-(route +) count + scan (one fused kernel) -> dispatch pack/scatter -> [expert
-stand-in, untimed] -> combine. The timed value is the device time of the
-layout + dispatch + combine kernels (CUDA events on the launching stream), with
+(route +) count (k_layout) + scan (k_scan) -> dispatch pack/scatter -> [expert
+stand-in, untimed] -> combine, launched with programmatic dependent launch. The
+timed value is the device time of the layout + dispatch phase plus the combine
+phase (CUDA events on the launching stream around each phase), with
 L2 flushed (a 320 MB write, then a 320 MB read so that no dirty line of the
 flush is written back inside a timed kernel) before the dispatch phase and
 again before the combine phase of every step, so every phase starts cold.
@@ -31,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "dispatch+combine us/layer (effective HBM GB/s vs GB300 peak in roofline)"
-KERNEL_SOURCES = {"k_layout": "layout.cu", "k_dispatch_bf16": "dispatch.cu",
+KERNEL_SOURCES = {"k_layout+k_scan": "layout.cu", "k_dispatch_bf16": "dispatch.cu",
                   "k_dispatch_fp8": "dispatch.cu", "k_combine": "combine.cu"}
 
 
@@ -284,17 +285,32 @@ def run_ours(args, wl, rank, world, local):
         else:
             layer.layout(ids, stream)
 
-    def step(ev, flush_before_combine=True, flush_before=True):
-        if flush_before:
+    def step(ev, flush=True):
+        """One layer; ev[0..3] bracket the layout+dispatch phase and the combine
+        phase (no event between the programmatically dependent launches)."""
+        if flush:
             flush_l2()
+        ev[0].record(stream)
+        layout()
+        layer.dispatch(x, w, stream)
+        ev[1].record(stream)
+        layer.expert(c, stream)
+        if flush:
+            flush_l2()
+        ev[2].record(stream)
+        layer.combine(w, stream)
+        ev[3].record(stream)
+
+    def step_diag(ev):
+        """The same layer with an event between every kernel (per-kernel times)."""
+        flush_l2()
         ev[0].record(stream)
         layout()
         ev[1].record(stream)
         layer.dispatch(x, w, stream)
         ev[2].record(stream)
         layer.expert(c, stream)
-        if flush_before_combine:
-            flush_l2()
+        flush_l2()
         ev[3].record(stream)
         layer.combine(w, stream)
         ev[4].record(stream)
@@ -306,7 +322,7 @@ def run_ours(args, wl, rank, world, local):
         step(ev)
     torch.cuda.synchronize(dev)
 
-    # cold: flush before each phase
+    # cold: L2 flushed before each phase
     evs = new_events(args.steps)
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -315,19 +331,25 @@ def run_ours(args, wl, rank, world, local):
             step(ev)
         torch.cuda.synchronize(dev)
     barrier(world)
-    lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dis_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    com_ms = [e[3].elapsed_time(e[4]) for e in evs]
-    step_ms = [a + b + d for a, b, d in zip(lay_ms, dis_ms, com_ms)]
+    step_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs]
     mean_ms = statistics.fmean(step_ms)
     mean_ms_all = max_over_ranks(mean_ms, world)
+
+    # per-kernel breakdown (events between kernels; diagnostic, same workload)
+    devs = new_events(min(args.steps, 50))
+    for ev in devs:
+        step_diag(ev)
+    torch.cuda.synchronize(dev)
+    lay_ms = [e[0].elapsed_time(e[1]) for e in devs]
+    dis_ms = [e[1].elapsed_time(e[2]) for e in devs]
+    com_ms = [e[3].elapsed_time(e[4]) for e in devs]
 
     # warm: no flushes (a layer right after the previous one; L2 keeps what fits)
     wevs = new_events(min(args.steps, 100))
     for ev in wevs:
-        step(ev, flush_before_combine=False, flush_before=False)
+        step(ev, flush=False)
     torch.cuda.synchronize(dev)
-    warm_ms = statistics.fmean([e[0].elapsed_time(e[2]) + e[3].elapsed_time(e[4]) for e in wevs])
+    warm_ms = statistics.fmean([e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in wevs])
 
     # end to end through the public API: pinned host inputs -> device, layer,
     # result -> pinned host, copies inside the timed region
@@ -366,10 +388,10 @@ def run_ours(args, wl, rank, world, local):
     kept = int(layer.layout_view()["totals"][0].item())
     kb = accounting.hbm_bytes(wl.P, wl.Tr, wl.E, wl.k, wl.H, layer.fp8, rows=kept, routed=routed)
     pay = accounting.payload_bytes(wl.P, wl.Tr, wl.k, wl.H, layer.fp8, rows=kept)
-    means = {"k_layout": statistics.fmean(lay_ms),
+    means = {"k_layout+k_scan": statistics.fmean(lay_ms),
              ("k_dispatch_fp8" if layer.fp8 else "k_dispatch_bf16"): statistics.fmean(dis_ms),
              "k_combine": statistics.fmean(com_ms)}
-    bytes_of = {"k_layout": kb.layout, "k_dispatch_fp8": kb.dispatch,
+    bytes_of = {"k_layout+k_scan": kb.layout, "k_dispatch_fp8": kb.dispatch,
                 "k_dispatch_bf16": kb.dispatch, "k_combine": kb.combine}
     dom = max(means, key=means.get)
     peak, peak_kind = hbm_peak()
@@ -399,7 +421,7 @@ def run_ours(args, wl, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
         "per_kernel_us": {k: round(v * 1e3, 3) for k, v in means.items()},
         "assignments_per_s": round(world * wl.Na / (mean_ms_all * 1e-3), 1),

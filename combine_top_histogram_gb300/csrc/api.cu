@@ -32,9 +32,11 @@ int validate(const moe_config_t* c) {
   if (c->dispatch_dtype == MOE_FP8_E4M3 && c->hidden % 128 != 0) return MOE_ERR_UNSUPPORTED;
   const long long T = (long long)c->num_ranks * c->tokens_per_rank;
   if (T * c->top_k >= (1ll << 31) - 1) return MOE_ERR_UNSUPPORTED;  // int32 row indices
-  // The layout kernel keeps its per-(source, expert) tables in shared memory.
+  // The layout kernels keep their per-warp counters and the per-(source,
+  // expert) tables in shared memory.
   if (moe::layout_smem_bytes(c->num_experts, moe::kMaxChunkAssign / c->top_k, c->top_k,
-                             c->num_ranks) > moe::kLayoutSmemLimit)
+                             c->num_ranks) > moe::kLayoutSmemLimit ||
+      moe::scan_smem_bytes(c->num_experts, c->num_ranks) > moe::kLayoutSmemLimit)
     return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -42,14 +44,14 @@ int validate(const moe_config_t* c) {
 struct Plan {
   int tpc_route, cps_route, tpc_ids, cps_ids, nchunks_max;
   size_t off_ctrl, off_totals, off_n_raw, off_n_kept, off_eoff, off_cnt, off_kept, off_C,
-      off_send, off_recv, off_rank, off_hist, off_acode, off_inv, bytes;
+      off_send, off_recv, off_rank, off_hist, off_pre, off_acode, off_inv, bytes;
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 // Chunking of the layout kernel. Given ids, a chunk of ~2048 assignments
 // keeps the scan short; when routing, chunks are cut smaller (down to one
-// token group per warp) so the top-k work spreads over about two CTAs per SM.
+// token per warp) so the top-k work spreads over about two CTAs per SM.
 Plan make_plan(const moe_config_t* c, int num_sms) {
   Plan p{};
   const int P = c->num_ranks, Tr = c->tokens_per_rank, E = c->num_experts, k = c->top_k;
@@ -61,11 +63,8 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   if (tpc > Tr) tpc = Tr;
   p.tpc_ids = tpc;
   p.cps_ids = ceil_div(Tr, tpc);
-  int k2 = 1;
-  while (k2 < k) k2 <<= 1;
-  const int group = 32 / k2;  // tokens one warp routes together
   int tr = (int)((T + 2ll * num_sms - 1) / (2ll * num_sms));
-  if (tr < moe::kLayoutWarps * group) tr = moe::kLayoutWarps * group;
+  if (tr < moe::kLayoutWarps) tr = moe::kLayoutWarps;  // at least one token per warp
   if (tr > 2048 / k) tr = 2048 / k;
   if (tr < 1) tr = 1;
   if (tr > max_tpc) tr = max_tpc;
@@ -93,6 +92,7 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   p.off_recv = take((size_t)P * E * 4);
   p.off_rank = take((size_t)(P + 1) * 4);
   p.off_hist = take((size_t)p.nchunks_max * E * 4);
+  p.off_pre = take((size_t)(P + 1) * E * 4);
   p.off_acode = take((size_t)Na * 4);
   p.off_inv = take((size_t)Na * 4);
   p.bytes = off;
@@ -112,6 +112,7 @@ moe::LayoutArgs layout_args(moe_handle_t h, bool route) {
   moe::LayoutArgs a{};
   a.acode = h->acode;
   a.hist = h->hist;
+  a.src_pre = h->src_pre;
   a.n_raw = h->n_raw;
   a.n_kept = h->n_kept;
   a.expert_offset = h->expert_offset;
@@ -204,6 +205,7 @@ int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
   h->recv_offset = reinterpret_cast<int32_t*>(ws + p.off_recv);
   h->rank_base = reinterpret_cast<int32_t*>(ws + p.off_rank);
   h->hist = reinterpret_cast<int32_t*>(ws + p.off_hist);
+  h->src_pre = reinterpret_cast<int32_t*>(ws + p.off_pre);
   h->acode = reinterpret_cast<int32_t*>(ws + p.off_acode);
   h->inv = reinterpret_cast<int32_t*>(ws + p.off_inv);
   if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess) {
@@ -298,6 +300,7 @@ int moe_dispatch(moe_handle_t h, const void* x, const float* w, void* recv_x, fl
   a.H = h->cfg.hidden;
   a.tpc = h->cur_tpc;
   a.cps = h->cur_cps;
+  a.nchunks = h->cfg.num_ranks * h->cur_cps;
   a.cap = h->cfg.expert_capacity;
   const int rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
   if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;

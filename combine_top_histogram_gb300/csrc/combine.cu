@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const CombineArgs p
   const int nvec = p.H >> 3;
   const int tid = threadIdx.x;
   const int k = K > 0 ? K : p.k;
+  pdl_wait();  // y (and inv, when dispatch ran just before) come from earlier kernels
+  pdl_trigger();
   for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
     if (tid < k) {
       rows_s[tid] = __ldg(p.inv + g * k + tid);
@@ -113,9 +115,9 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const CombineArgs p
 template <int K>
 cudaError_t launch_combine_k(const CombineArgs& a, int blocks, cudaStream_t st) {
   const int nvec = a.H >> 3;
-  if (nvec <= 128) k_combine<K, 1><<<blocks, kCombineThreads, 0, st>>>(a);
-  else if (nvec <= 512) k_combine<K, 4><<<blocks, kCombineThreads, 0, st>>>(a);
-  else k_combine<K, 8><<<blocks, kCombineThreads, 0, st>>>(a);
+  if (nvec <= 128) return launch_pdl(k_combine<K, 1>, dim3(blocks), dim3(kCombineThreads), 0, st, a);
+  else if (nvec <= 512) return launch_pdl(k_combine<K, 4>, dim3(blocks), dim3(kCombineThreads), 0, st, a);
+  else return launch_pdl(k_combine<K, 8>, dim3(blocks), dim3(kCombineThreads), 0, st, a);
   return cudaGetLastError();
 }
 
@@ -124,6 +126,8 @@ cudaError_t launch_combine_k(const CombineArgs& a, int blocks, cudaStream_t st) 
 __global__ void __launch_bounds__(128) k_standin(const StandinArgs p) {
   __shared__ float c_s;
   const int nvec = p.H >> 3;
+  pdl_wait();
+  pdl_trigger();
   const int total = __ldg(p.expert_offset + p.E);
   for (long long r = blockIdx.x; r < total && r < p.rows_max; r += gridDim.x) {
     if (threadIdx.x == 0) {
@@ -191,8 +195,7 @@ cudaError_t launch_standin(const StandinArgs& a, int num_sms, cudaStream_t st) {
   long long blocks = a.rows_max;
   const long long cap = (long long)num_sms * 16;
   if (blocks > cap) blocks = cap;
-  k_standin<<<(int)blocks, 128, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_standin, dim3((int)blocks), dim3(128), 0, st, a);
 }
 
 }  // namespace moe

@@ -49,7 +49,7 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
     const int s = (int)(g / p.Tr);
     const int t = (int)(g - (long long)s * p.Tr);
     const int b = s * p.cps + t / p.tpc;
-    const int pos = __ldg(p.hist + (long long)b * p.E + e) + code_rank(code);
+    const int pos = __ldg(p.hist + (long long)e * p.nchunks + b) + code_rank(code);
     if (p.cap <= 0 || pos < p.cap) {
       r = __ldg(p.expert_offset + e) + pos;
       p.m_local_expert[r] = e % p.L;
@@ -68,9 +68,8 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_bf16(const Dispat
   __shared__ int rows_s[MOE_MAX_TOPK];
   const int nvec = p.H >> 3;  // 16-byte vectors per row
   const int tid = threadIdx.x;
+  bool waited = false;
   for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
-    resolve_rows(p, g, rows_s);
-    __syncthreads();
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -78,6 +77,16 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_bf16(const Dispat
       for (int i = 0; i < VPT; ++i) {
         const int v = v0 + i * kDispatchThreads + tid;
         if (v < nvec) val[i] = ld_stream(src + v);
+      }
+      if (v0 == 0) {
+        // x is an input of the path: its first loads overlap the layout's tail
+        if (!waited) {
+          pdl_wait();
+          pdl_trigger();
+          waited = true;
+        }
+        resolve_rows(p, g, rows_s);
+        __syncthreads();
       }
       for (int j = 0; j < p.k; ++j) {
         const int r = rows_s[j];
@@ -135,9 +144,8 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const Dispatc
   const int nvec = p.H >> 3;
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
+  bool waited = false;
   for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
-    resolve_rows(p, g, rows_s);
-    __syncthreads();
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -147,6 +155,18 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const Dispatc
       for (int i = 0; i < VPT; ++i) {
         const int v = v0 + i * kDispatchThreads + tid;
         val[i] = v < nvec ? ld_stream(src + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (v0 == 0) {
+        if (!waited) {
+          pdl_wait();
+          pdl_trigger();
+          waited = true;
+        }
+        resolve_rows(p, g, rows_s);
+        __syncthreads();
+      }
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
         float m = amax8(val[i]);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -181,13 +201,13 @@ cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaSt
   if (blocks > cap) blocks = cap;
   const int nvec = a.H >> 3;
   if (fp8) {
-    if (nvec <= 128) k_dispatch_fp8<1><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
-    else if (nvec <= 512) k_dispatch_fp8<4><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
-    else k_dispatch_fp8<8><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+    if (nvec <= 128) return launch_pdl(k_dispatch_fp8<1>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
+    else if (nvec <= 512) return launch_pdl(k_dispatch_fp8<4>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
+    else return launch_pdl(k_dispatch_fp8<8>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
   } else {
-    if (nvec <= 128) k_dispatch_bf16<1><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
-    else if (nvec <= 512) k_dispatch_bf16<4><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
-    else k_dispatch_bf16<8><<<(int)blocks, kDispatchThreads, 0, st>>>(a);
+    if (nvec <= 128) return launch_pdl(k_dispatch_bf16<1>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
+    else if (nvec <= 512) return launch_pdl(k_dispatch_bf16<4>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
+    else return launch_pdl(k_dispatch_bf16<8>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
   }
   return cudaGetLastError();
 }

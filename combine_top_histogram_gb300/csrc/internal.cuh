@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_ep.h"
 
 namespace moe {
@@ -16,10 +18,9 @@ constexpr int kLayoutWarps = kLayoutThreads / 32;
 // Assignments per layout chunk are bounded so that a chunk-local rank fits in
 // the low 16 bits of an assignment code (code = expert << 16 | rank).
 constexpr int kMaxChunkAssign = 4096;
-// The device-wide scan stages the chunk table through shared memory in tiles
-// of this many int32 (16 per thread); E must not exceed it.
-constexpr int kScanTile = kLayoutThreads * 16;
-// Shared memory the layout kernel may use per CTA (GB300: 227 KB opt-in).
+// Column-scan kernel shape: one warp per expert.
+constexpr int kScanThreads = 512;
+// Shared memory the layout kernels may use per CTA (GB300: 227 KB opt-in).
 constexpr size_t kLayoutSmemLimit = 220 * 1024;
 
 // Per-assignment code written by the layout kernel and read by dispatch:
@@ -34,7 +35,8 @@ struct LayoutArgs {
   int32_t* ids_out;       // [T*k] routed ids (route mode)
   float* w_out;           // [T*k] routed weights (route mode)
   int32_t* acode;         // [T*k] assignment codes
-  int32_t* hist;          // [nchunks*E]: chunk counts, then exclusive chunk bases
+  int32_t* hist;          // [E][nchunks]: chunk counts, then exclusive chunk bases
+  int32_t* src_pre;       // [(P+1)*E]: prefix of expert e at source s's first chunk
   int32_t* n_raw;         // [E]
   int32_t* n_kept;        // [E]
   int32_t* expert_offset; // [E+1]
@@ -57,7 +59,7 @@ struct DispatchArgs {
   const uint16_t* x;      // bf16 bits [T*H]
   const float* w;         // [T*k]
   const int32_t* acode;   // [T*k]
-  const int32_t* hist;    // [nchunks*E] exclusive chunk bases
+  const int32_t* hist;    // [E][nchunks] exclusive chunk bases
   const int32_t* expert_offset;
   int32_t* inv;           // [T*k]
   void* recv;             // bf16 [rows*H] or e4m3 [rows*H]
@@ -68,7 +70,7 @@ struct DispatchArgs {
   int32_t* m_slot;
   float* m_weight;
   long long T;
-  int Tr, k, E, L, H, tpc, cps, cap;
+  int Tr, k, E, L, H, tpc, cps, nchunks, cap;
 };
 
 struct CombineArgs {
@@ -90,11 +92,40 @@ struct StandinArgs {
   int E, H, fp8;
 };
 
+// Programmatic dependent launch: every kernel of the path is launched with
+// programmatic stream serialization, waits for its predecessor grid
+// (griddepcontrol.wait) before reading anything the predecessor may write, and
+// right after that lets its own dependents launch (their CTAs then wait in
+// hardware). Because a kernel triggers only after its own wait, data written
+// two or more launches earlier is complete whenever a kernel starts, so it may
+// be read before the wait. Without the launch attribute the wait is a no-op.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_layout(const LayoutArgs& a, bool route, int num_sms, cudaStream_t st);
 cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long long T,
                               int E, int k, int num_sms, cudaStream_t st);
 size_t layout_smem_bytes(int E, int tpc, int k, int P);
+size_t scan_smem_bytes(int E, int P);
 cudaError_t layout_prepare(int E, int tpc, int k, int P);
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
@@ -117,6 +148,6 @@ struct moe_handle {
   uint32_t* done;           // ctrl[1]
   int32_t* totals;          // [4]
   int32_t *n_raw, *n_kept, *expert_offset, *cnt, *kept_cnt, *C, *send_offset,
-      *recv_offset, *rank_base, *hist, *acode, *inv;
+      *recv_offset, *rank_base, *hist, *src_pre, *acode, *inv;
   unsigned long long layout_gen, dispatch_gen;
 };

@@ -110,14 +110,18 @@ __device__ __forceinline__ float key_value(unsigned k) {
 // the keys and one min-reduction of the tied candidates' expert indices.
 // Register i of a lane holds expert i*32 + lane. Lane j < k returns slot j.
 template <int EPL>
-__device__ __forceinline__ void topk_select(const float* __restrict__ z, int E, int k, int lane,
-                                            int& out_id, float& out_z) {
-  unsigned key[EPL];
+__device__ __forceinline__ void load_keys(const float* __restrict__ z, int E, int lane,
+                                          unsigned (&key)[EPL]) {
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = i * 32 + lane;
     key[i] = e < E ? order_key(__ldg(z + e)) : 0u;
   }
+}
+
+template <int EPL>
+__device__ __forceinline__ void topk_select(unsigned (&key)[EPL], int k, int lane, int& out_id,
+                                            float& out_z) {
   out_id = -1;
   out_z = 0.0f;
   for (int j = 0; j < k; ++j) {
@@ -162,16 +166,26 @@ __device__ __forceinline__ void route_group_warp(const float* __restrict__ logit
   valid = grp < ntok && slot < k;
   id = -1;
   float my_z = 0.0f;
-  for (int t = 0; t < ntok; ++t) {
-    int tid_;
-    float tz;
-    topk_select<EPL>(logits + (g0 + t) * (long long)E, E, k, lane, tid_, tz);
-    const int src = slot < 32 ? slot : 0;
-    const int sid = __shfl_sync(kFull, tid_, src);
-    const float sz = __shfl_sync(kFull, tz, src);
-    if (grp == t) {
-      id = sid;
-      my_z = sz;
+  // The logits of up to kPre tokens are loaded before any is selected.
+  constexpr int kPre = EPL >= 32 ? 1 : (32 / EPL < 4 ? 32 / EPL : 4);
+  for (int t0 = 0; t0 < ntok; t0 += kPre) {
+    unsigned key[kPre][EPL];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u)
+      if (t0 + u < ntok) load_keys<EPL>(logits + (g0 + t0 + u) * (long long)E, E, lane, key[u]);
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      if (t0 + u < ntok) {
+        int tid_;
+        float tz;
+        topk_select<EPL>(key[u], k, lane, tid_, tz);
+        const int sid = __shfl_sync(kFull, tid_, slot);
+        const float sz = __shfl_sync(kFull, tz, slot);
+        if (grp == t0 + u) {
+          id = sid;
+          my_z = sz;
+        }
+      }
     }
   }
   const float z0 = __shfl_sync(kFull, my_z, lane & ~(K2 - 1));
@@ -195,124 +209,89 @@ __device__ __forceinline__ void route_group_warp(const float* __restrict__ logit
   }
 }
 
-// Device-wide scan by the last chunk CTA. The chunk table [nchunks][E] is
-// staged through shared memory in tiles of kScanTile ints (coalesced loads, the
-// next tile's loads in flight while the current one is scanned); each thread
-// owns expert columns and carries the running count across tiles. The
-// per-(source, expert) prefixes at source boundaries, the kept counts and the
-// count matrix stay in shared memory, so no step walks global memory serially.
-__device__ void layout_scan(const LayoutArgs& p, int* tile, int* rest) {
-  const int E = p.E, P = p.P, tid = threadIdx.x;
-  constexpr int NT = kLayoutThreads;
-  constexpr int PER = kScanTile / NT;  // staged values per thread per tile
-  int* run = rest;                  // [E]        running column sums
-  int* pre = run + E;               // [(P+1)*E]  prefix at each source's first chunk
-  int* sk = pre + (P + 1) * E;      // [E]        kept counts -> expert offsets
-  int* Cs = sk + E;                 // [P*P]      count matrix
+// The layout tables, by the last CTA of the scan kernel: reads n_kept,
+// n_raw and the per-(source, expert) prefixes into shared memory, scans the
+// kept counts in global expert order (expert offsets) and derives every
+// per-(source, expert) and per-(source, rank) table and the totals.
+__device__ void layout_tables(const LayoutArgs& p, int* smem) {
+  const int E = p.E, P = p.P, tid = threadIdx.x, NT = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int* sk = smem;                   // [E]        kept counts -> expert offsets
+  int* sraw = sk + E;               // [E]
+  int* pre = sraw + E;              // [(P+1)*E]  prefix at each source's first chunk
+  int* Cs = pre + (P + 1) * E;      // [P*P]      count matrix
   int* tmp = Cs + P * P;            // [32]
   int* red = tmp + 32;              // [2]        dropped, raw total
-
-  const int TB = kScanTile / E;     // chunks per tile (E <= kScanTile)
-  for (int e = tid; e < E; e += NT) run[e] = 0;
   if (tid < 2) red[tid] = 0;
-
-  int stage[PER];
-  auto load_tile = [&](int b0) {
-    const int n = min(TB, p.nchunks - b0) * E;
-    const int* src = p.hist + (long long)b0 * E;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int i = q * NT + tid;
-      stage[q] = i < n ? __ldcg(src + i) : 0;
-    }
-  };
-  load_tile(0);
-  for (int b0 = 0; b0 < p.nchunks; b0 += TB) {
-    const int nb = min(TB, p.nchunks - b0);
-    const int n = nb * E;
-    __syncthreads();  // previous tile fully stored / run[] initialised
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int i = q * NT + tid;
-      if (i < n) tile[i] = stage[q];
-    }
-    __syncthreads();
-    if (b0 + TB < p.nchunks) load_tile(b0 + TB);  // consumed next iteration
-    const int s_first = (b0 + p.cps - 1) / p.cps;  // first source starting in this tile
-    for (int e = tid; e < E; e += NT) {
-      int r = run[e];
-      int s_next = s_first, b_next = s_first * p.cps;
-      for (int bb = 0; bb < nb; ++bb) {
-        if (b0 + bb == b_next) {  // first chunk of source s_next
-          pre[s_next * E + e] = r;
-          ++s_next;
-          b_next += p.cps;
-        }
-        const int v = tile[bb * E + e];
-        tile[bb * E + e] = r;
-        r += v;
-      }
-      run[e] = r;
-    }
-    __syncthreads();
-    int* dst = p.hist + (long long)b0 * E;
-    for (int i = tid; i < n; i += NT) dst[i] = tile[i];
+  for (int e = tid; e < E; e += NT) {
+    sk[e] = __ldcg(p.n_kept + e);
+    sraw[e] = __ldcg(p.n_raw + e);
   }
+  for (int i = tid; i < (P + 1) * E; i += NT) pre[i] = __ldcg(p.src_pre + i);
   __syncthreads();
-  // Per-expert totals, capacity clamp.
   {
     int dr = 0, rw = 0;
     for (int e = tid; e < E; e += NT) {
-      const int raw = run[e];
-      const int kept = (p.cap > 0 && raw > p.cap) ? p.cap : raw;
-      pre[P * E + e] = raw;
-      sk[e] = kept;
-      p.n_raw[e] = raw;
-      p.n_kept[e] = kept;
-      rw += raw;
-      dr += raw - kept;
+      rw += sraw[e];
+      dr += sraw[e] - sk[e];
     }
     if (dr) atomicAdd(&red[0], dr);
     if (rw) atomicAdd(&red[1], rw);
   }
-  __syncthreads();
   // Expert offsets: exclusive scan of kept counts in global expert order.
   const int total = cta_exclusive_scan(sk, E, tmp);
   for (int e = tid; e <= E; e += NT) p.expert_offset[e] = e < E ? sk[e] : total;
+  for (int d = tid; d <= P; d += NT) p.rank_base[d] = d < P ? sk[d * p.L] : total;
+  auto kept_of = [&](int s, int e) {
+    const int a = pre[s * E + e];
+    const int c = pre[(s + 1) * E + e] - a;
+    return p.cap > 0 ? min(max(p.cap - a, 0), c) : c;
+  };
   // Per (source, expert): raw and kept counts, receive offsets.
   for (int it = tid; it < P * E; it += NT) {
     const int s = it / E, e = it - s * E;
     const int a = pre[s * E + e];
-    const int c = pre[(s + 1) * E + e] - a;
-    int kept = c, start = a;
-    if (p.cap > 0) {
-      kept = min(max(p.cap - a, 0), c);
-      start = min(a, p.cap);
-    }
-    p.cnt[it] = c;
-    p.kept_cnt[it] = kept;
-    p.recv_offset[it] = sk[e] + start;
+    p.cnt[it] = pre[(s + 1) * E + e] - a;
+    p.kept_cnt[it] = kept_of(s, e);
+    p.recv_offset[it] = sk[e] + (p.cap > 0 ? min(a, p.cap) : a);
   }
-  // Count matrix C[s][d]: kept assignments of source s to the experts of d.
-  for (int it = tid; it < P * P; it += NT) {
-    const int s = it / P, d = it - s * P;
-    int sum = 0;
-    for (int e = d * p.L; e < (d + 1) * p.L; ++e) {
-      const int a = pre[s * E + e];
-      const int c = pre[(s + 1) * E + e] - a;
-      sum += p.cap > 0 ? min(max(p.cap - a, 0), c) : c;
+  // Count matrix C[s][d] = kept assignments of source s to the experts of d:
+  // one thread per (s, d) for few local experts, one warp per (s, d) for many.
+  if (p.L < 64) {
+    for (int it = tid; it < P * P; it += NT) {
+      const int s = it / P, d = it - s * P;
+      int sum = 0;
+      for (int e = d * p.L; e < (d + 1) * p.L; ++e) sum += kept_of(s, e);
+      Cs[it] = sum;
+      p.C[it] = sum;
     }
-    Cs[it] = sum;
-    p.C[it] = sum;
+  } else {
+    for (int it = warp; it < P * P; it += NT / 32) {
+      const int s = it / P, d = it - s * P;
+      int sum = 0;
+      for (int e = d * p.L + lane; e < (d + 1) * p.L; e += 32) sum += kept_of(s, e);
+      sum = __reduce_add_sync(kFull, sum);
+      if (lane == 0) {
+        Cs[it] = sum;
+        p.C[it] = sum;
+      }
+    }
   }
-  for (int d = tid; d <= P; d += NT) p.rank_base[d] = d < P ? sk[d * p.L] : total;
   __syncthreads();
-  // Send offsets: exclusive prefix of C[s][.] over destinations.
-  for (int s = tid; s < P; s += NT) {
-    int r = 0;
-    for (int d = 0; d < P; ++d) {
-      p.send_offset[(long long)s * P + d] = r;
-      r += Cs[s * P + d];
+  // Send offsets: exclusive prefix of C[s][.] over destinations, one warp per s.
+  for (int s = warp; s < P; s += NT / 32) {
+    int carry = 0;
+    for (int d0 = 0; d0 < P; d0 += 32) {
+      const int d = d0 + lane;
+      const int v = d < P ? Cs[s * P + d] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      if (d < P) p.send_offset[(long long)s * P + d] = carry + x - v;
+      carry += __shfl_sync(kFull, x, 31);
     }
   }
   if (tid == 0) {
@@ -324,16 +303,59 @@ __device__ void layout_scan(const LayoutArgs& p, int* tile, int* rest) {
   }
 }
 
+// Column scan of the chunk histograms, one warp per expert: the table is
+// [E][nchunks], so a warp reads its expert's column contiguously, turns it
+// into exclusive chunk bases in place (warp shuffle scan, carried across
+// 32-chunk steps), and records the prefix at each source rank's first chunk
+// and the expert's totals. The last CTA to arrive builds the tables.
+__global__ void __launch_bounds__(kScanThreads) k_scan(const LayoutArgs p) {
+  extern __shared__ int smem[];
+  __shared__ int s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x * (kScanThreads / 32) + warp;
+  pdl_wait();
+  pdl_trigger();
+  if (e < p.E) {
+    int* col = p.hist + (long long)e * p.nchunks;
+    int carry = 0;
+    for (int c0 = 0; c0 < p.nchunks; c0 += 32) {
+      const int b = c0 + lane;
+      const int v = b < p.nchunks ? __ldcg(col + b) : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      const int excl = carry + x - v;
+      if (b < p.nchunks) {
+        col[b] = excl;
+        if (b % p.cps == 0) p.src_pre[(b / p.cps) * p.E + e] = excl;
+      }
+      carry += __shfl_sync(kFull, x, 31);
+    }
+    if (lane == 0) {
+      p.src_pre[p.P * p.E + e] = carry;
+      p.n_raw[e] = carry;
+      p.n_kept[e] = (p.cap > 0 && carry > p.cap) ? p.cap : carry;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(p.done, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  layout_tables(p, smem);
+}
+
 template <bool ROUTE, int EPL>
 __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
   extern __shared__ int smem[];
-  __shared__ int s_last;
   const int E = p.E;
-  // Region A: per-warp expert counters, later the scan's staging tile.
-  // Region B: the chunk's expert ids, later the scan's tables.
   int* wcnt = smem;                                         // [warps][E]
   const int wcnt_ints = kLayoutWarps * E;
-  int* ids_s = smem + (wcnt_ints > kScanTile ? wcnt_ints : kScanTile);  // [tpc*k]
+  int* ids_s = smem + wcnt_ints;                            // [tpc*k]
 
   const int b = blockIdx.x;
   const int s = b / p.cps, c = b - s * p.cps;
@@ -345,11 +367,15 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   for (int i = tid; i < wcnt_ints; i += kLayoutThreads) wcnt[i] = 0;
+  pdl_wait();  // logits / ids may come from the previous kernel
+  pdl_trigger();
 
   if (ROUTE) {
     int K2 = 1;
     while (K2 < p.k) K2 <<= 1;
-    const int G = 32 / K2;  // tokens routed together by one warp
+    // tokens routed together by one warp: one when the chunk is small (latency),
+    // up to 32/K2 when there are many (fewer instructions per token)
+    const int G = min(32 / K2, (nt + kLayoutWarps - 1) / kLayoutWarps);
     for (int tl0 = warp * G; tl0 < nt; tl0 += kLayoutWarps * G) {
       bool valid;
       int id;
@@ -395,7 +421,7 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
       wcnt[w * E + e] = run;
       run += v;
     }
-    p.hist[(long long)b * E + e] = run;
+    p.hist[(long long)e * p.nchunks + b] = run;  // transposed: [E][nchunks]
   }
   __syncthreads();
   // Pass 2: stable rank of every assignment within the chunk and expert.
@@ -412,14 +438,6 @@ __global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
     if (i < end) p.acode[a0 + i] = code;
   }
 
-  // Arrival: the last chunk CTA performs the device-wide scan.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(p.done, 1u) == (unsigned)(p.nchunks - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  layout_scan(p, smem, ids_s);
 }
 
 template <int EPL>
@@ -427,6 +445,8 @@ __global__ void __launch_bounds__(256) k_route_only(const float* __restrict__ lo
                                                     int32_t* ids, float* w, long long T, int E,
                                                     int k) {
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   int K2 = 1;
   while (K2 < k) K2 <<= 1;
   const int G = 32 / K2;
@@ -466,11 +486,12 @@ int experts_per_lane(int E) {
 
 }  // namespace
 
-size_t layout_smem_bytes(int E, int tpc, int k, int P) {
-  const size_t a = (size_t)(kLayoutWarps * E > kScanTile ? kLayoutWarps * E : kScanTile);
-  const size_t tables = (size_t)E + (size_t)(P + 1) * E + E + (size_t)P * P + 34;
-  const size_t ids = (size_t)tpc * k;
-  return sizeof(int) * (a + (tables > ids ? tables : ids));
+size_t layout_smem_bytes(int E, int tpc, int k, int /*P*/) {
+  return sizeof(int) * ((size_t)kLayoutWarps * E + (size_t)tpc * k);
+}
+
+size_t scan_smem_bytes(int E, int P) {
+  return sizeof(int) * ((size_t)2 * E + (size_t)(P + 1) * E + (size_t)P * P + 34);
 }
 
 // The dynamic shared-memory limit is a per-kernel setting shared by every
@@ -478,20 +499,25 @@ size_t layout_smem_bytes(int E, int tpc, int k, int P) {
 // lowered to one configuration's need); the launch itself asks for what the
 // configuration uses.
 cudaError_t layout_prepare(int E, int tpc, int k, int P) {
-  const size_t smem = layout_smem_bytes(E, tpc, k, P);
   int dev = 0, optin = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (err != cudaSuccess) return err;
   const int epl = experts_per_lane(E);
-  for (void* fn : {layout_kernel_ptr<true>(epl), layout_kernel_ptr<false>(epl)}) {
+  struct {
+    void* fn;
+    size_t need;
+  } kernels[] = {{layout_kernel_ptr<true>(epl), layout_smem_bytes(E, tpc, k, P)},
+                 {layout_kernel_ptr<false>(epl), layout_smem_bytes(E, tpc, k, P)},
+                 {(void*)k_scan, scan_smem_bytes(E, P)}};
+  for (auto& kd : kernels) {
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, fn);
+    err = cudaFuncGetAttributes(&fa, kd.fn);
     if (err != cudaSuccess) return err;
     const int dyn_max = optin - (int)fa.sharedSizeBytes;  // static shared memory counts too
-    if (smem > (size_t)dyn_max) return cudaErrorInvalidValue;
-    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
+    if (kd.need > (size_t)dyn_max) return cudaErrorInvalidValue;
+    err = cudaFuncSetAttribute(kd.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;
@@ -501,9 +527,12 @@ cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cuda
   const size_t smem = layout_smem_bytes(a.E, a.tpc, a.k, a.P);
   const int epl = experts_per_lane(a.E);
   void* fn = route ? layout_kernel_ptr<true>(epl) : layout_kernel_ptr<false>(epl);
-  LayoutArgs args = a;
-  void* params[] = {&args};
-  return cudaLaunchKernel(fn, dim3(a.nchunks), dim3(kLayoutThreads), params, smem, st);
+  cudaError_t err = launch_pdl(reinterpret_cast<void (*)(const LayoutArgs)>(fn), dim3(a.nchunks),
+                               dim3(kLayoutThreads), smem, st, a);
+  if (err != cudaSuccess) return err;
+  const int scan_blocks = (a.E + kScanThreads / 32 - 1) / (kScanThreads / 32);
+  return launch_pdl(k_scan, dim3(scan_blocks), dim3(kScanThreads), scan_smem_bytes(a.E, a.P), st,
+                    a);
 }
 
 cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long long T, int E,
@@ -514,12 +543,12 @@ cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long 
   const long long cap = (long long)num_sms * 8;
   if (blocks > cap) blocks = cap;
   switch (experts_per_lane(E)) {
-    case 1: k_route_only<1><<<(int)blocks, 256, 0, st>>>(logits, ids, w, T, E, k); break;
-    case 2: k_route_only<2><<<(int)blocks, 256, 0, st>>>(logits, ids, w, T, E, k); break;
-    case 4: k_route_only<4><<<(int)blocks, 256, 0, st>>>(logits, ids, w, T, E, k); break;
-    case 8: k_route_only<8><<<(int)blocks, 256, 0, st>>>(logits, ids, w, T, E, k); break;
-    case 16: k_route_only<16><<<(int)blocks, 256, 0, st>>>(logits, ids, w, T, E, k); break;
-    default: k_route_only<32><<<(int)blocks, 256, 0, st>>>(logits, ids, w, T, E, k); break;
+    case 1: return launch_pdl(k_route_only<1>, dim3((int)blocks), dim3(256), 0, st, logits, ids, w, T, E, k);
+    case 2: return launch_pdl(k_route_only<2>, dim3((int)blocks), dim3(256), 0, st, logits, ids, w, T, E, k);
+    case 4: return launch_pdl(k_route_only<4>, dim3((int)blocks), dim3(256), 0, st, logits, ids, w, T, E, k);
+    case 8: return launch_pdl(k_route_only<8>, dim3((int)blocks), dim3(256), 0, st, logits, ids, w, T, E, k);
+    case 16: return launch_pdl(k_route_only<16>, dim3((int)blocks), dim3(256), 0, st, logits, ids, w, T, E, k);
+    default: return launch_pdl(k_route_only<32>, dim3((int)blocks), dim3(256), 0, st, logits, ids, w, T, E, k);
   }
   return cudaGetLastError();
 }

@@ -48,7 +48,8 @@ void* scratch_address(int device) {
 __global__ void k_inv_from_codes(const int32_t* __restrict__ acode,
                                  const int32_t* __restrict__ hist,
                                  const int32_t* __restrict__ expert_offset, int32_t* inv,
-                                 long long Na, int k, int Tr, int E, int tpc, int cps, int cap) {
+                                 long long Na, int k, int Tr, int E, int tpc, int cps, int cap,
+                                 int nchunks) {
   for (long long a = (long long)blockIdx.x * blockDim.x + threadIdx.x; a < Na;
        a += (long long)gridDim.x * blockDim.x) {
     const int code = acode[a];
@@ -58,7 +59,7 @@ __global__ void k_inv_from_codes(const int32_t* __restrict__ acode,
       const long long g = a / k;
       const int s = (int)(g / Tr);
       const int t = (int)(g - (long long)s * Tr);
-      const int pos = hist[(long long)(s * cps + t / tpc) * E + e] + moe::code_rank(code);
+      const int pos = hist[(long long)e * nchunks + (s * cps + t / tpc)] + moe::code_rank(code);
       if (cap <= 0 || pos < cap) r = expert_offset[e] + pos;
     }
     inv[a] = r;
@@ -98,9 +99,10 @@ extern "C" int moe_dispatch_layout_noalloc(const moe_config_t* cfg, const int32_
   if (tpc > Tr) tpc = Tr;
   const int cps = (Tr + tpc - 1) / tpc;
   const int nchunks = P * cps;
-  // Scratch map: [control words][chunk histograms][assignment codes].
+  // Scratch map: [control words][chunk histograms][source prefixes][codes].
   const size_t off_hist = 256;
-  const size_t off_codes = off_hist + round256((size_t)nchunks * E * 4);
+  const size_t off_pre = off_hist + round256((size_t)nchunks * E * 4);
+  const size_t off_codes = off_pre + round256((size_t)(P + 1) * E * 4);
   const size_t need = off_codes + round256((size_t)Na * 4);
   if (need > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
 
@@ -118,6 +120,7 @@ extern "C" int moe_dispatch_layout_noalloc(const moe_config_t* cfg, const int32_
   a.ids_in = ids;
   a.acode = reinterpret_cast<int32_t*>(base + off_codes);
   a.hist = reinterpret_cast<int32_t*>(base + off_hist);
+  a.src_pre = reinterpret_cast<int32_t*>(base + off_pre);
   a.n_raw = out->expert_count_raw;
   a.n_kept = out->expert_count;
   a.expert_offset = out->expert_offset;
@@ -148,6 +151,7 @@ extern "C" int moe_dispatch_layout_noalloc(const moe_config_t* cfg, const int32_
   if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
   if (blocks < 1) blocks = 1;
   k_inv_from_codes<<<(int)blocks, 256, 0, st>>>(a.acode, a.hist, out->expert_offset, out->inv,
-                                                Na, k, Tr, E, tpc, cps, cfg->expert_capacity);
+                                                Na, k, Tr, E, tpc, cps, cfg->expert_capacity,
+                                                nchunks);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

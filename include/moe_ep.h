@@ -44,6 +44,13 @@
  *     treated as masked. Capacity drops are counted, not errors.
  *   - Token rows are bf16 [T, H] row-major; T = P*T_r; global token
  *     g = s*T_r + t; assignment a = g*k + j (slot j of token g).
+ *   - Kernels are launched with programmatic dependent launch: each waits for
+ *     the previous grid on the stream before reading what that grid may have
+ *     written, and lets its successor launch right after that wait.
+ *     moe_dispatch starts loading x before its wait, so x must not be written
+ *     by the immediately preceding kernel on the stream if that kernel lets
+ *     its dependents launch before it finishes (kernels launched without
+ *     programmatic dependent launch, and this library's own kernels, are fine).
  */
 #ifndef MOE_EP_H
 #define MOE_EP_H
@@ -222,7 +229,8 @@ int moe_combine(moe_handle_t h, const void *y, const float *w, void *out,
  * called. Intermediate data lives in one file-scope device array of
  * MOE_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
  * until the process exits; a problem whose scratch (256 + 4*E*P*ceil(T_r/c)
- * + 4*T*k bytes, each term rounded up to 256, c = chunk tokens) exceeds it
+ * + 4*E*(P+1) + 4*T*k bytes, each term rounded up to 256, c = chunk tokens)
+ * exceeds it
  * returns MOE_ERR_UNSUPPORTED and enqueues nothing.
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
