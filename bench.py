@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="override T_r (a smaller case of the same workload, e.g. for ncu)")
     return ap.parse_args()
 
 
@@ -441,6 +443,10 @@ def main():
     if args.config not in W.CONFIGS:
         raise SystemExit(f"unknown --config {args.config}; choose from {list(W.CONFIGS)}")
     wl = W.CONFIGS[args.config]
+    if args.tokens_per_rank:
+        tr = args.tokens_per_rank
+        cap = W.prefill_capacity(wl.P * tr, wl.k, wl.E) if wl.cap else 0
+        wl = wl.scaled(f"{wl.name}_tr{tr}", Tr=tr, cap=cap)
     rank, world, local = dist_init(args.gpus)
     try:
         if args.impl == "reference":
