@@ -256,6 +256,7 @@ def run_ours(args, wl, rank, world, local):
     import torch
 
     from combine_top_histogram_gb300 import MoeLayer, accounting
+    from combine_top_histogram_gb300 import binding as B
     from combine_top_histogram_gb300 import workloads as W
 
     dev = torch.device("cuda", local)
@@ -370,9 +371,9 @@ def run_ours(args, wl, rank, world, local):
     for i, ev in enumerate(eevs):
         flush_l2()
         ev[0].record(stream)
-        x.copy_(x_h, non_blocking=True)
+        B.moe_copy_h2d_async(x, x_h, stream)
         for a, b in zip(r_d, r_h):
-            a.copy_(b, non_blocking=True)
+            B.moe_copy_h2d_async(a, b, stream)
         layout()
         layer.dispatch(x, w, stream)
         ev[1].record(stream)
@@ -380,7 +381,7 @@ def run_ours(args, wl, rank, world, local):
         flush_l2()
         ev[2].record(stream)
         layer.combine(w, stream)
-        out_h.copy_(layer.out, non_blocking=True)
+        B.moe_copy_d2h_async(out_h, layer.out, stream)
         ev[3].record(stream)
     torch.cuda.synchronize(dev)
     for ev in eevs[3:]:

@@ -30,7 +30,7 @@ EXPORTED_SYMBOLS = (
     "moe_workspace_bytes", "moe_recv_rows_max", "moe_handle_create", "moe_handle_destroy",
     "moe_route_topk", "moe_dispatch_layout", "moe_route_dispatch_layout", "moe_get_layout",
     "moe_dispatch", "moe_expert_standin", "moe_combine", "moe_read_status", "moe_error_string",
-    "moe_dispatch_layout_noalloc",
+    "moe_dispatch_layout_noalloc", "moe_copy_h2d_async", "moe_copy_d2h_async",
 )
 
 
@@ -106,6 +106,10 @@ def load_library():
         lib.moe_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp]
         lib.moe_dispatch_layout_noalloc.restype = i32
         lib.moe_dispatch_layout_noalloc.argtypes = [cfgp, vp, ctypes.POINTER(moe_layout_view_t), vp]
+        lib.moe_copy_h2d_async.restype = i32
+        lib.moe_copy_h2d_async.argtypes = [vp, vp, sz, vp]
+        lib.moe_copy_d2h_async.restype = i32
+        lib.moe_copy_d2h_async.argtypes = [vp, vp, sz, vp]
         lib.moe_error_string.restype = ctypes.c_char_p
         lib.moe_error_string.argtypes = [i32]
         _lib = lib
@@ -261,6 +265,32 @@ def moe_dispatch_layout_noalloc(cfg: moe_config_t, ids, out: dict, stream=None) 
     v = moe_layout_view_t(*(_ptr(out[n]) for n, _ in moe_layout_view_t._fields_))
     _check("moe_dispatch_layout_noalloc", load_library().moe_dispatch_layout_noalloc(
         ctypes.byref(cfg), _ptr(ids), ctypes.byref(v), _stream(stream)))
+
+
+def _host_ptr(t) -> int:
+    if t.is_cuda:
+        raise ValueError("expected a host tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def moe_copy_h2d_async(dst, src_host, stream=None) -> None:
+    """Stream-ordered copy of a (pinned) host tensor into a device tensor."""
+    n = src_host.numel() * src_host.element_size()
+    if n != dst.numel() * dst.element_size():
+        raise ValueError("size mismatch")
+    _check("moe_copy_h2d_async", load_library().moe_copy_h2d_async(
+        _ptr(dst), _host_ptr(src_host), n, _stream(stream)))
+
+
+def moe_copy_d2h_async(dst_host, src, stream=None) -> None:
+    """Stream-ordered copy of a device tensor into a (pinned) host tensor."""
+    n = src.numel() * src.element_size()
+    if n != dst_host.numel() * dst_host.element_size():
+        raise ValueError("size mismatch")
+    _check("moe_copy_d2h_async", load_library().moe_copy_d2h_async(
+        _host_ptr(dst_host), _ptr(src), n, _stream(stream)))
 
 
 def moe_error_string(code: int) -> str:

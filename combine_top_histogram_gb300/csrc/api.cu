@@ -352,6 +352,20 @@ int moe_read_status(moe_handle_t h, uint32_t* flags, void* stream) {
   return MOE_OK;
 }
 
+int moe_copy_h2d_async(void* dst_device, const void* src_host, size_t bytes, void* stream) {
+  if ((!dst_device || !src_host) && bytes) return MOE_ERR_INVALID_ARG;
+  if (!bytes) return MOE_OK;
+  return cuda_rc(cudaMemcpyAsync(dst_device, src_host, bytes, cudaMemcpyHostToDevice,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int moe_copy_d2h_async(void* dst_host, const void* src_device, size_t bytes, void* stream) {
+  if ((!dst_host || !src_device) && bytes) return MOE_ERR_INVALID_ARG;
+  if (!bytes) return MOE_OK;
+  return cuda_rc(cudaMemcpyAsync(dst_host, src_device, bytes, cudaMemcpyDeviceToHost,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_error_string(int code) {
   switch (code) {
     case MOE_OK: return "ok";

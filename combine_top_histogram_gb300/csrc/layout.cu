@@ -257,7 +257,7 @@ __device__ void layout_tables(const LayoutArgs& p, int* smem) {
   }
   // Count matrix C[s][d] = kept assignments of source s to the experts of d:
   // one thread per (s, d) for few local experts, one warp per (s, d) for many.
-  if (p.L < 64) {
+  if (p.L < 16) {
     for (int it = tid; it < P * P; it += NT) {
       const int s = it / P, d = it - s * P;
       int sum = 0;

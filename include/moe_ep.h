@@ -243,6 +243,16 @@ int moe_combine(moe_handle_t h, const void *y, const float *w, void *out,
 int moe_dispatch_layout_noalloc(const moe_config_t *cfg, const int32_t *ids,
                                 const moe_layout_view_t *out, void *stream);
 
+/* ---- host <-> device staging ---------------------------------------------
+ * Asynchronous copies on `stream` with the copy engines (cudaMemcpyAsync),
+ * for callers whose tokens live in host memory: copy x / logits / ids / w in
+ * before the layer and the restored rows out after it, all stream-ordered.
+ * Host buffers should be page-locked for the copies to be asynchronous.
+ * The pages have no counterpart for these two utilities. Errors: INVALID_ARG
+ * (null pointer), CUDA. */
+int moe_copy_h2d_async(void *dst_device, const void *src_host, size_t bytes, void *stream);
+int moe_copy_d2h_async(void *dst_host, const void *src_device, size_t bytes, void *stream);
+
 /* Reads and clears the device status word. Synchronises `stream`: tests and
  * debugging only. *flags receives MOE_STATUS_* bits. */
 int moe_read_status(moe_handle_t h, uint32_t *flags, void *stream);

@@ -221,3 +221,17 @@ def test_errors_and_call_order(gpu):
     with pytest.raises(B.MoeError) as ei:
         B.Handle(B.make_config(2, 4, 8, 2, 64), small)
     assert ei.value.code == -3
+
+
+def test_host_copy_utilities(gpu):
+    import torch
+    from combine_top_histogram_gb300 import binding as B
+    src = torch.arange(1 << 20, dtype=torch.int32).pin_memory()
+    dev = torch.empty_like(src, device="cuda")
+    back = torch.empty_like(src).pin_memory()
+    B.moe_copy_h2d_async(dev, src)
+    B.moe_copy_d2h_async(back, dev)
+    torch.cuda.synchronize()
+    assert torch.equal(back, src)
+    with pytest.raises(ValueError):
+        B.moe_copy_h2d_async(dev[:10], src)
