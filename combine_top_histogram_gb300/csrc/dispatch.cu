@@ -106,20 +106,18 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_bf16(const Dispat
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-__device__ __forceinline__ uint32_t e4m3_byte(float v) {
-  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-}
-
-// Quantises 8 bf16 values (one 16-byte vector) with scale s; returns 8 codes.
+// Quantises 8 bf16 values (one 16-byte vector) with scale s; returns the 8
+// codes e4m3_satfinite_rne(x / s), the quotient an IEEE division; the codes
+// are converted two per instruction (.x in the low byte).
 __device__ __forceinline__ uint2 quant8(const uint4 x, float s, bool zero_block) {
   if (zero_block) return make_uint2(0u, 0u);
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
   uint32_t out[2] = {0u, 0u};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint32_t c0 = e4m3_byte(__fdiv_rn(bf16_lo(w[q]), s));
-    const uint32_t c1 = e4m3_byte(__fdiv_rn(bf16_hi(w[q]), s));
-    out[q >> 1] |= (c0 | (c1 << 8)) << (16 * (q & 1));
+    const float2 qq = make_float2(__fdiv_rn(bf16_lo(w[q]), s), __fdiv_rn(bf16_hi(w[q]), s));
+    const uint32_t c = (uint32_t)__nv_cvt_float2_to_fp8x2(qq, __NV_SATFINITE, __NV_E4M3);
+    out[q >> 1] |= c << (16 * (q & 1));
   }
   return make_uint2(out[0], out[1]);
 }

@@ -235,3 +235,27 @@ def test_host_copy_utilities(gpu):
     assert torch.equal(back, src)
     with pytest.raises(ValueError):
         B.moe_copy_h2d_async(dev[:10], src)
+
+
+def test_fp8_quotients_at_e4m3_rounding_boundaries(gpu):
+    """Blocks whose quotients x/s land exactly on, or one bf16 step around,
+    e4m3 rounding boundaries (midpoints between neighbouring codes), with a
+    power-of-two scale (exact quotients, ties to even) and inexact scales."""
+    import oracle
+    wl = W.Workload("fp8mid", 2, 8, 4, 2, 1024, W.MOE_FP8_E4M3, "uniform", "dequant", seed=11)
+    inp = W.make_inputs(wl)
+    reps = np.array([oracle.e4m3_value(c) for c in range(0x7F)], np.float64)
+    mids = (reps[:-1] + reps[1:]) / 2
+    rng = np.random.default_rng(12)
+    vals = np.zeros((wl.T, wl.H), np.float32)
+    for t in range(wl.T):
+        for blk in range(wl.H // 128):
+            amax = [56.0, 447.0, 3.0, 0.0371][(t + blk) % 4]  # s = amax / 448
+            s = np.float32(np.float32(amax) / np.float32(448.0))
+            m = rng.choice(mids, 127) * rng.choice([-1.0, 1.0], 127)
+            x = (m * np.float64(s)).astype(np.float32)
+            x *= np.float32(1.0) + np.float32(2.0 ** -8) * rng.integers(-1, 2, 127).astype(np.float32)
+            row = np.concatenate([[amax], x]).astype(np.float32)
+            vals[t, blk * 128:(blk + 1) * 128] = row
+    inp.x[:] = W._bf16_bits_from_f32(vals)
+    _check(wl, inp)
