@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--dispatch", default="fused", choices=["fused", "two_stage"],
+                    help="two_stage: the pack + separate all-to-all-v comparator")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override T_r (a smaller case of the same workload, e.g. for ncu)")
     return ap.parse_args()
@@ -288,6 +290,12 @@ def run_ours(args, wl, rank, world, local):
         else:
             layer.layout(ids, stream)
 
+    def dispatch():
+        if args.dispatch == "two_stage":
+            layer.dispatch_two_stage(x, w, stream)
+        else:
+            layer.dispatch(x, w, stream)
+
     def step(ev, flush=True):
         """One layer; ev[0..3] bracket the layout+dispatch phase and the combine
         phase (no event between the programmatically dependent launches)."""
@@ -295,7 +303,7 @@ def run_ours(args, wl, rank, world, local):
             flush_l2()
         ev[0].record(stream)
         layout()
-        layer.dispatch(x, w, stream)
+        dispatch()
         ev[1].record(stream)
         layer.expert(c, stream)
         if flush:
@@ -310,7 +318,7 @@ def run_ours(args, wl, rank, world, local):
         ev[0].record(stream)
         layout()
         ev[1].record(stream)
-        layer.dispatch(x, w, stream)
+        dispatch()
         ev[2].record(stream)
         layer.expert(c, stream)
         flush_l2()
@@ -375,7 +383,7 @@ def run_ours(args, wl, rank, world, local):
         for a, b in zip(r_d, r_h):
             B.moe_copy_h2d_async(a, b, stream)
         layout()
-        layer.dispatch(x, w, stream)
+        dispatch()
         ev[1].record(stream)
         layer.expert(c, stream)
         flush_l2()
@@ -391,15 +399,16 @@ def run_ours(args, wl, rank, world, local):
     kept = int(layer.layout_view()["totals"][0].item())
     kb = accounting.hbm_bytes(wl.P, wl.Tr, wl.E, wl.k, wl.H, layer.fp8, rows=kept, routed=routed)
     pay = accounting.payload_bytes(wl.P, wl.Tr, wl.k, wl.H, layer.fp8, rows=kept)
-    means = {"k_layout+k_scan": statistics.fmean(lay_ms),
-             ("k_dispatch_fp8" if layer.fp8 else "k_dispatch_bf16"): statistics.fmean(dis_ms),
+    dkey = "k_dispatch_fp8" if layer.fp8 else "k_dispatch_bf16"
+    if args.dispatch == "two_stage":
+        dkey = "two_stage(k_send_pos+" + dkey + "+k_a2av)"
+    means = {"k_layout+k_scan": statistics.fmean(lay_ms), dkey: statistics.fmean(dis_ms),
              "k_combine": statistics.fmean(com_ms)}
-    bytes_of = {"k_layout+k_scan": kb.layout, "k_dispatch_fp8": kb.dispatch,
-                "k_dispatch_bf16": kb.dispatch, "k_combine": kb.combine}
+    bytes_of = {"k_layout+k_scan": kb.layout, dkey: kb.dispatch, "k_combine": kb.combine}
     dom = max(means, key=means.get)
     peak, peak_kind = hbm_peak()
     achieved = bytes_of[dom] / (means[dom] * 1e-3) / 1e9
-    traffic = committed_traffic(dom, wl.name)
+    traffic = committed_traffic(dom, wl.name) if dom in KERNEL_SOURCES else None
     cpu = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
         s, desc, n, _ = oracle_layer_seconds(wl, args.cpu_seconds)
@@ -416,7 +425,7 @@ def run_ours(args, wl, rank, world, local):
                    "top_k": wl.k, "hidden": wl.H, "capacity": wl.cap,
                    "l2": "flushed (320 MB write, then 320 MB read) before the dispatch and "
                          "the combine phase of every timed step",
-                   "replicas": world},
+                   "replicas": world, "dispatch": args.dispatch},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,

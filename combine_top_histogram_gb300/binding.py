@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "moe_route_topk", "moe_dispatch_layout", "moe_route_dispatch_layout", "moe_get_layout",
     "moe_dispatch", "moe_expert_standin", "moe_combine", "moe_read_status", "moe_error_string",
     "moe_dispatch_layout_noalloc", "moe_copy_h2d_async", "moe_copy_d2h_async",
+    "moe_dispatch_two_stage",
 )
 
 
@@ -98,6 +99,9 @@ def load_library():
         lib.moe_get_layout.argtypes = [vp, ctypes.POINTER(moe_layout_view_t)]
         lib.moe_dispatch.restype = i32
         lib.moe_dispatch.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(moe_recv_meta_t), vp]
+        lib.moe_dispatch_two_stage.restype = i32
+        lib.moe_dispatch_two_stage.argtypes = [vp, vp, vp, vp, vp, vp, vp,
+                                               ctypes.POINTER(moe_recv_meta_t), vp]
         lib.moe_expert_standin.restype = i32
         lib.moe_expert_standin.argtypes = [vp, vp, vp, vp, vp, vp]
         lib.moe_combine.restype = i32
@@ -237,6 +241,15 @@ def moe_dispatch(h: Handle, x, w, recv_x, recv_scale, meta: dict, stream=None) -
     _check("moe_dispatch", load_library().moe_dispatch(
         h.ptr, _ptr(x), _ptr(w), _ptr(recv_x), _ptr(recv_scale), ctypes.byref(m),
         _stream(stream)))
+
+
+def moe_dispatch_two_stage(h: Handle, x, w, send_x, send_scale, recv_x, recv_scale, meta: dict,
+                           stream=None) -> None:
+    m = moe_recv_meta_t(*(_ptr(meta[n]) for n in (
+        "local_expert", "src_rank", "src_token", "slot", "weight")))
+    _check("moe_dispatch_two_stage", load_library().moe_dispatch_two_stage(
+        h.ptr, _ptr(x), _ptr(w), _ptr(send_x), _ptr(send_scale), _ptr(recv_x), _ptr(recv_scale),
+        ctypes.byref(m), _stream(stream)))
 
 
 def moe_expert_standin(h: Handle, recv_x, recv_scale, expert_scale, y, stream=None) -> None:

@@ -44,7 +44,8 @@ int validate(const moe_config_t* c) {
 struct Plan {
   int tpc_route, cps_route, tpc_ids, cps_ids, nchunks_max;
   size_t off_ctrl, off_totals, off_n_raw, off_n_kept, off_eoff, off_cnt, off_kept, off_C,
-      off_send, off_recv, off_rank, off_hist, off_pre, off_acode, off_inv, bytes;
+      off_send, off_recv, off_rank, off_hist, off_pre, off_acode, off_inv, off_spos, off_sbase,
+      bytes;
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -95,6 +96,8 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   p.off_pre = take((size_t)(P + 1) * E * 4);
   p.off_acode = take((size_t)Na * 4);
   p.off_inv = take((size_t)Na * 4);
+  p.off_spos = take((size_t)P * E * 4);
+  p.off_sbase = take((size_t)(P + 1) * 4);
   p.bytes = off;
   return p;
 }
@@ -208,6 +211,8 @@ int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
   h->src_pre = reinterpret_cast<int32_t*>(ws + p.off_pre);
   h->acode = reinterpret_cast<int32_t*>(ws + p.off_acode);
   h->inv = reinterpret_cast<int32_t*>(ws + p.off_inv);
+  h->send_pos = reinterpret_cast<int32_t*>(ws + p.off_spos);
+  h->src_base = reinterpret_cast<int32_t*>(ws + p.off_sbase);
   if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
@@ -303,6 +308,68 @@ int moe_dispatch(moe_handle_t h, const void* x, const float* w, void* recv_x, fl
   a.nchunks = h->cfg.num_ranks * h->cur_cps;
   a.cap = h->cfg.expert_capacity;
   const int rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
+  if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
+  return rc;
+}
+
+int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* send_x,
+                           float* send_scale, void* recv_x, float* recv_scale,
+                           const moe_recv_meta_t* meta, void* stream) {
+  if (!h || !x || !w || !send_x || !recv_x || !meta) return MOE_ERR_INVALID_ARG;
+  if (!meta->local_expert || !meta->src_rank || !meta->src_token || !meta->slot || !meta->weight)
+    return MOE_ERR_INVALID_ARG;
+  const bool fp8 = h->cfg.dispatch_dtype == MOE_FP8_E4M3;
+  if (fp8 && (!recv_scale || !send_scale)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(send_x, 16)) return MOE_ERR_INVALID_ARG;
+  if (h->layout_gen == 0) return MOE_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = cuda_rc(moe::launch_send_pos(h->kept_cnt, h->send_pos, h->src_base,
+                                        h->cfg.num_ranks, h->cfg.num_experts, st));
+  if (rc != MOE_OK) return rc;
+  moe::DispatchArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.w = w;
+  a.acode = h->acode;
+  a.hist = h->hist;
+  a.expert_offset = h->expert_offset;
+  a.inv = h->inv;
+  a.recv = send_x;
+  a.recv_scale = send_scale;
+  a.m_local_expert = meta->local_expert;
+  a.m_src_rank = meta->src_rank;
+  a.m_src_token = meta->src_token;
+  a.m_slot = meta->slot;
+  a.m_weight = meta->weight;
+  a.T = h->T;
+  a.Tr = h->cfg.tokens_per_rank;
+  a.k = h->cfg.top_k;
+  a.E = h->cfg.num_experts;
+  a.L = h->L;
+  a.H = h->cfg.hidden;
+  a.tpc = h->cur_tpc;
+  a.cps = h->cur_cps;
+  a.nchunks = h->cfg.num_ranks * h->cur_cps;
+  a.cap = h->cfg.expert_capacity;
+  a.send_pos = h->send_pos;
+  a.src_base = h->src_base;
+  a.recv_offset = h->recv_offset;
+  rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, st));
+  if (rc != MOE_OK) return rc;
+  moe::A2avArgs c{};
+  c.send = send_x;
+  c.send_scale = fp8 ? send_scale : nullptr;
+  c.recv = recv_x;
+  c.recv_scale = recv_scale;
+  c.expert_offset = h->expert_offset;
+  c.recv_offset = h->recv_offset;
+  c.send_pos = h->send_pos;
+  c.src_base = h->src_base;
+  c.rows_max = h->rows_max;
+  c.row_bytes = (long long)h->cfg.hidden * (fp8 ? 1 : 2);
+  c.P = h->cfg.num_ranks;
+  c.E = h->cfg.num_experts;
+  c.nblk = h->cfg.hidden / 128;
+  rc = cuda_rc(moe::launch_a2av(c, h->num_sms, st));
   if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
   return rc;
 }

@@ -60,7 +60,12 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
     }
   }
   p.inv[a] = r;
-  rows_s[j] = r;
+  int dst = r;
+  if (p.send_pos && r >= 0) {
+    const long long se = (long long)code_expert(code) + (long long)(g / p.Tr) * p.E;
+    dst = __ldg(p.src_base + g / p.Tr) + __ldg(p.send_pos + se) + (r - __ldg(p.recv_offset + se));
+  }
+  rows_s[j] = dst;
 }
 
 template <int VPT>

@@ -71,6 +71,26 @@ struct DispatchArgs {
   float* m_weight;
   long long T;
   int Tr, k, E, L, H, tpc, cps, nchunks, cap;
+  // Two-stage comparator: when send_pos is set, payload rows go to the send
+  // pool row src_base[s] + send_pos[s][e] + (r - recv_offset[s][e]) instead of
+  // the receive row r (metadata and inv still describe receive rows).
+  const int32_t* send_pos;
+  const int32_t* src_base;
+  const int32_t* recv_offset;
+};
+
+struct A2avArgs {
+  const void* send;          // send pool rows
+  const float* send_scale;   // FP8 scale rows of the send pool, or null
+  void* recv;
+  float* recv_scale;
+  const int32_t* expert_offset;
+  const int32_t* recv_offset;
+  const int32_t* send_pos;
+  const int32_t* src_base;
+  long long rows_max;
+  long long row_bytes;       // payload bytes per row (multiple of 16)
+  int P, E, nblk;
 };
 
 struct CombineArgs {
@@ -130,6 +150,9 @@ cudaError_t layout_prepare(int E, int tpc, int k, int P);
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_standin(const StandinArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_send_pos(const int32_t* kept_cnt, int32_t* send_pos, int32_t* src_base, int P,
+                            int E, cudaStream_t st);
+cudaError_t launch_a2av(const A2avArgs& a, int num_sms, cudaStream_t st);
 
 }  // namespace moe
 
@@ -148,6 +171,6 @@ struct moe_handle {
   uint32_t* done;           // ctrl[1]
   int32_t* totals;          // [4]
   int32_t *n_raw, *n_kept, *expert_offset, *cnt, *kept_cnt, *C, *send_offset,
-      *recv_offset, *rank_base, *hist, *src_pre, *acode, *inv;
+      *recv_offset, *rank_base, *hist, *src_pre, *acode, *inv, *send_pos, *src_base;
   unsigned long long layout_gen, dispatch_gen;
 };

@@ -54,6 +54,17 @@ class MoeLayer:
     def dispatch(self, x, w, stream=None):
         B.moe_dispatch(self.handle, x, w, self.recv_x, self.recv_scale, self.meta, stream)
 
+    def dispatch_two_stage(self, x, w, stream=None):
+        """The two-stage comparator: pack into per-source send buffers, then a
+        separate all-to-all-v copy into the same receive layout."""
+        import torch
+        if getattr(self, "send_x", None) is None:
+            self.send_x = torch.empty_like(self.recv_x)
+            self.send_scale = (torch.empty_like(self.recv_scale)
+                               if self.recv_scale is not None else None)
+        B.moe_dispatch_two_stage(self.handle, x, w, self.send_x, self.send_scale, self.recv_x,
+                                 self.recv_scale, self.meta, stream)
+
     def expert(self, expert_scale=None, stream=None):
         B.moe_expert_standin(self.handle, self.recv_x, self.recv_scale, expert_scale, self.y,
                              stream)
@@ -61,14 +72,19 @@ class MoeLayer:
     def combine(self, w, stream=None):
         B.moe_combine(self.handle, self.y, w, self.out, stream)
 
-    def forward(self, x, ids=None, w=None, logits=None, expert_scale=None, stream=None):
-        """Whole layer; with logits the routed ids/weights land in self.ids / self.w."""
+    def forward(self, x, ids=None, w=None, logits=None, expert_scale=None, stream=None,
+                two_stage=False):
+        """Whole layer; with logits the routed ids/weights land in self.ids / self.w.
+        two_stage=True dispatches through the two-stage comparator."""
         if logits is not None:
             self.route_layout(logits, stream)
             w = self.w
         else:
             self.layout(ids, stream)
-        self.dispatch(x, w, stream)
+        if two_stage:
+            self.dispatch_two_stage(x, w, stream)
+        else:
+            self.dispatch(x, w, stream)
         self.expert(expert_scale, stream)
         self.combine(w, stream)
         return self.out

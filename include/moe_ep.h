@@ -199,6 +199,18 @@ int moe_get_layout(moe_handle_t h, moe_layout_view_t *out);
 int moe_dispatch(moe_handle_t h, const void *x, const float *w, void *recv_x,
                  float *recv_scale, const moe_recv_meta_t *meta, void *stream);
 
+/* NEXT-row comparator, the "standard" two-stage dispatch ([A2A] 4.3 and 5.2):
+ * stage 1 packs every kept assignment into its source rank's send buffer
+ * ([to rank 0][to rank 1]..., each destination segment bucketed by local
+ * expert, (token, slot) order inside), stage 2 is a separate all-to-all-v copy
+ * of each (source, expert) segment into the receive regions. Produces exactly
+ * what moe_dispatch produces (same receive rows, metadata and inv), through one
+ * more full write + read of the payload. send_x: rows_max rows like recv_x;
+ * send_scale: rows_max x H/128 fp32 for FP8 (NULL for BF16). */
+int moe_dispatch_two_stage(moe_handle_t h, const void *x, const float *w, void *send_x,
+                           float *send_scale, void *recv_x, float *recv_scale,
+                           const moe_recv_meta_t *meta, void *stream);
+
 /* a6 -- expert stand-in (the pages' grouped GEMM is out of scope): for every
  * kept receive row r of expert e, y[r] = bf16(c[e] * x_r), where x_r is the
  * bf16 payload (c = NULL means c[e] = 1) or, for FP8, the dequantised value
