@@ -45,8 +45,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--dispatch", default="fused", choices=["fused", "two_stage"],
-                    help="two_stage: the pack + separate all-to-all-v comparator")
+    ap.add_argument("--dispatch", default="separate", choices=["separate", "fused", "two_stage"],
+                    help="separate: layout kernels then the dispatch kernel; fused: one "
+                         "persistent launch; two_stage: the pack + all-to-all-v comparator")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override T_r (a smaller case of the same workload, e.g. for ncu)")
     return ap.parse_args()
@@ -293,8 +294,15 @@ def run_ours(args, wl, rank, world, local):
     def dispatch():
         if args.dispatch == "two_stage":
             layer.dispatch_two_stage(x, w, stream)
-        else:
+        elif args.dispatch == "separate":
             layer.dispatch(x, w, stream)
+
+    if args.dispatch == "fused":  # layout and dispatch are one launch
+        def layout():
+            if routed:
+                layer.layout_dispatch_fused(x, logits=logits, stream=stream)
+            else:
+                layer.layout_dispatch_fused(x, ids=ids, w=w, stream=stream)
 
     def step(ev, flush=True):
         """One layer; ev[0..3] bracket the layout+dispatch phase and the combine
@@ -400,11 +408,18 @@ def run_ours(args, wl, rank, world, local):
     kb = accounting.hbm_bytes(wl.P, wl.Tr, wl.E, wl.k, wl.H, layer.fp8, rows=kept, routed=routed)
     pay = accounting.payload_bytes(wl.P, wl.Tr, wl.k, wl.H, layer.fp8, rows=kept)
     dkey = "k_dispatch_fp8" if layer.fp8 else "k_dispatch_bf16"
+    lkey = "k_layout+k_scan"
     if args.dispatch == "two_stage":
         dkey = "two_stage(k_send_pos+" + dkey + "+k_a2av)"
-    means = {"k_layout+k_scan": statistics.fmean(lay_ms), dkey: statistics.fmean(dis_ms),
-             "k_combine": statistics.fmean(com_ms)}
-    bytes_of = {"k_layout+k_scan": kb.layout, dkey: kb.dispatch, "k_combine": kb.combine}
+    if args.dispatch == "fused":
+        lkey = "k_fused(route+layout+dispatch)"
+        means = {lkey: statistics.fmean([a + b for a, b in zip(lay_ms, dis_ms)]),
+                 "k_combine": statistics.fmean(com_ms)}
+        bytes_of = {lkey: kb.layout + kb.dispatch, "k_combine": kb.combine}
+    else:
+        means = {lkey: statistics.fmean(lay_ms), dkey: statistics.fmean(dis_ms),
+                 "k_combine": statistics.fmean(com_ms)}
+        bytes_of = {lkey: kb.layout, dkey: kb.dispatch, "k_combine": kb.combine}
     dom = max(means, key=means.get)
     peak, peak_kind = hbm_peak()
     achieved = bytes_of[dom] / (means[dom] * 1e-3) / 1e9
@@ -433,7 +448,8 @@ def run_ours(args, wl, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (2 if args.dispatch == "fused" else
+                         6 if args.dispatch == "two_stage" else 4) * args.steps,
         "clocks": clk.summary(),
         "per_kernel_us": {k: round(v * 1e3, 3) for k, v in means.items()},
         "assignments_per_s": round(world * wl.Na / (mean_ms_all * 1e-3), 1),

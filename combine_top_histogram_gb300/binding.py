@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "moe_route_topk", "moe_dispatch_layout", "moe_route_dispatch_layout", "moe_get_layout",
     "moe_dispatch", "moe_expert_standin", "moe_combine", "moe_read_status", "moe_error_string",
     "moe_dispatch_layout_noalloc", "moe_copy_h2d_async", "moe_copy_d2h_async",
-    "moe_dispatch_two_stage",
+    "moe_dispatch_two_stage", "moe_layout_dispatch_fused", "moe_set_wait_limit",
 )
 
 
@@ -102,6 +102,11 @@ def load_library():
         lib.moe_dispatch_two_stage.restype = i32
         lib.moe_dispatch_two_stage.argtypes = [vp, vp, vp, vp, vp, vp, vp,
                                                ctypes.POINTER(moe_recv_meta_t), vp]
+        lib.moe_layout_dispatch_fused.restype = i32
+        lib.moe_layout_dispatch_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp,
+                                                  ctypes.POINTER(moe_recv_meta_t), vp]
+        lib.moe_set_wait_limit.restype = i32
+        lib.moe_set_wait_limit.argtypes = [vp, ctypes.c_int64]
         lib.moe_expert_standin.restype = i32
         lib.moe_expert_standin.argtypes = [vp, vp, vp, vp, vp, vp]
         lib.moe_combine.restype = i32
@@ -250,6 +255,20 @@ def moe_dispatch_two_stage(h: Handle, x, w, send_x, send_scale, recv_x, recv_sca
     _check("moe_dispatch_two_stage", load_library().moe_dispatch_two_stage(
         h.ptr, _ptr(x), _ptr(w), _ptr(send_x), _ptr(send_scale), _ptr(recv_x), _ptr(recv_scale),
         ctypes.byref(m), _stream(stream)))
+
+
+def moe_layout_dispatch_fused(h: Handle, logits, ids, w, x, recv_x, recv_scale, meta: dict,
+                              stream=None) -> None:
+    """Route (logits given) or take ids/w, lay out and dispatch in one launch."""
+    m = moe_recv_meta_t(*(_ptr(meta[n]) for n in (
+        "local_expert", "src_rank", "src_token", "slot", "weight")))
+    _check("moe_layout_dispatch_fused", load_library().moe_layout_dispatch_fused(
+        h.ptr, _ptr(logits), _ptr(ids), _ptr(w), _ptr(x), _ptr(recv_x), _ptr(recv_scale),
+        ctypes.byref(m), _stream(stream)))
+
+
+def moe_set_wait_limit(h: Handle, polls: int) -> None:
+    _check("moe_set_wait_limit", load_library().moe_set_wait_limit(h.ptr, int(polls)))
 
 
 def moe_expert_standin(h: Handle, recv_x, recv_scale, expert_scale, y, stream=None) -> None:

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmoe_ep.so")
-SOURCES = ["api.cu", "layout.cu", "dispatch.cu", "combine.cu", "layout_noalloc.cu", "two_stage.cu"]
+SOURCES = ["api.cu", "layout.cu", "dispatch.cu", "combine.cu", "layout_noalloc.cu", "two_stage.cu",
+           "fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -74,6 +74,7 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   p.cps_route = ceil_div(Tr, tr);
   const int n1 = P * p.cps_ids, n2 = P * p.cps_route;
   p.nchunks_max = n1 > n2 ? n1 : n2;
+  if (p.nchunks_max < num_sms) p.nchunks_max = num_sms;  // persistent path: one chunk per SM
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -213,6 +214,7 @@ int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
   h->inv = reinterpret_cast<int32_t*>(ws + p.off_inv);
   h->send_pos = reinterpret_cast<int32_t*>(ws + p.off_spos);
   h->src_base = reinterpret_cast<int32_t*>(ws + p.off_sbase);
+  h->wait_limit = 1ll << 22;  // ~0.3 s of 64 ns polls
   if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
@@ -372,6 +374,86 @@ int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* 
   rc = cuda_rc(moe::launch_a2av(c, h->num_sms, st));
   if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
   return rc;
+}
+
+int moe_set_wait_limit(moe_handle_t h, int64_t polls) {
+  if (!h || polls < 0) return MOE_ERR_INVALID_ARG;
+  h->wait_limit = polls;
+  return MOE_OK;
+}
+
+int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids, float* w,
+                              const void* x, void* recv_x, float* recv_scale,
+                              const moe_recv_meta_t* meta, void* stream) {
+  if (!h || !ids || !w || !x || !recv_x || !meta) return MOE_ERR_INVALID_ARG;
+  if (!meta->local_expert || !meta->src_rank || !meta->src_token || !meta->slot || !meta->weight)
+    return MOE_ERR_INVALID_ARG;
+  const bool fp8 = h->cfg.dispatch_dtype == MOE_FP8_E4M3;
+  const bool route = logits != nullptr;
+  if (fp8 && !recv_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv_x, 16)) return MOE_ERR_INVALID_ARG;
+  const int P = h->cfg.num_ranks, Tr = h->cfg.tokens_per_rank, E = h->cfg.num_experts,
+            k = h->cfg.top_k, H = h->cfg.hidden;
+  // One CTA per SM; chunks of whole tokens of one source rank, one per CTA.
+  const int grid = h->num_sms;
+  int cps = grid / P;
+  if (cps < 1) return MOE_ERR_UNSUPPORTED;
+  int tpc = ceil_div(Tr, cps);
+  cps = ceil_div(Tr, tpc);
+  if ((long long)tpc * k > moe::kMaxChunkAssign || P * cps > h->nchunks_max) return MOE_ERR_UNSUPPORTED;
+  const bool prefetch = (size_t)tpc * H * 2 <= (size_t)144 * 1024;
+  int xs_off = 0;
+  const size_t smem = moe::fused_smem_bytes(E, tpc, k, H, P, prefetch, &xs_off);
+  int per_sm = 0;
+  if (moe::fused_prepare(route, fp8, E, smem, &per_sm) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
+  moe::FusedArgs f{};
+  f.lay = layout_args(h, route);
+  f.lay.ids_in = ids;
+  f.lay.logits = logits;
+  f.lay.ids_out = ids;
+  f.lay.w_out = w;
+  f.lay.tpc = tpc;
+  f.lay.cps = cps;
+  f.lay.nchunks = P * cps;
+  moe::DispatchArgs& a = f.dis;
+  a.x = static_cast<const uint16_t*>(x);
+  a.w = w;
+  a.acode = h->acode;
+  a.hist = h->hist;
+  a.expert_offset = h->expert_offset;
+  a.inv = h->inv;
+  a.recv = recv_x;
+  a.recv_scale = recv_scale;
+  a.m_local_expert = meta->local_expert;
+  a.m_src_rank = meta->src_rank;
+  a.m_src_token = meta->src_token;
+  a.m_slot = meta->slot;
+  a.m_weight = meta->weight;
+  a.T = h->T;
+  a.Tr = Tr;
+  a.k = k;
+  a.E = E;
+  a.L = h->L;
+  a.H = H;
+  a.tpc = tpc;
+  a.cps = cps;
+  a.nchunks = P * cps;
+  a.cap = h->cfg.expert_capacity;
+  f.bar = h->status + 4;
+  f.wait_limit = h->wait_limit;
+  f.prefetch_x = prefetch ? 1 : 0;
+  f.xs_offset_ints = xs_off;
+  const int rc = cuda_rc(moe::launch_fused(f, route, fp8, grid, smem, static_cast<cudaStream_t>(stream)));
+  if (rc != MOE_OK) return rc;
+  h->cur_tpc = tpc;
+  h->cur_cps = cps;
+  h->layout_gen += 1;
+  h->dispatch_gen = h->layout_gen;
+  return MOE_OK;
 }
 
 int moe_expert_standin(moe_handle_t h, const void* recv_x, const float* recv_scale,

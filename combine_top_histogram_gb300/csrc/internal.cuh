@@ -79,6 +79,16 @@ struct DispatchArgs {
   const int32_t* recv_offset;
 };
 
+// Persistent single-launch route/layout/dispatch (fused.cu).
+struct FusedArgs {
+  LayoutArgs lay;
+  DispatchArgs dis;
+  unsigned* bar;          // 3 counters: grid barrier 1, grid barrier 2, exit
+  long long wait_limit;   // polls before a grid barrier gives up
+  int prefetch_x;         // x rows staged in shared memory during the layout
+  int xs_offset_ints;     // where they start in dynamic shared memory
+};
+
 struct A2avArgs {
   const void* send;          // send pool rows
   const float* send_scale;   // FP8 scale rows of the send pool, or null
@@ -153,6 +163,11 @@ cudaError_t launch_standin(const StandinArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_send_pos(const int32_t* kept_cnt, int32_t* send_pos, int32_t* src_base, int P,
                             int E, cudaStream_t st);
 cudaError_t launch_a2av(const A2avArgs& a, int num_sms, cudaStream_t st);
+size_t fused_smem_bytes(int E, int tpc, int k, int H, int P, bool prefetch_x,
+                        int* xs_offset_ints);
+cudaError_t fused_prepare(bool route, bool fp8, int E, size_t smem, int* blocks_per_sm);
+cudaError_t launch_fused(const FusedArgs& f, bool route, bool fp8, int grid, size_t smem,
+                         cudaStream_t st);
 
 }  // namespace moe
 
@@ -173,4 +188,5 @@ struct moe_handle {
   int32_t *n_raw, *n_kept, *expert_offset, *cnt, *kept_cnt, *C, *send_offset,
       *recv_offset, *rank_base, *hist, *src_pre, *acode, *inv, *send_pos, *src_base;
   unsigned long long layout_gen, dispatch_gen;
+  long long wait_limit;     // bounded device waits (persistent path)
 };

@@ -1,0 +1,374 @@
+// layout_device.cuh -- device-side pieces of the layout shared by the
+// separate layout kernels (layout.cu) and the persistent single-launch path
+// (fused.cu): warp top-k routing with float-float softmax weights, ballot peer
+// masks, CTA scans, the per-chunk count/rank body and the layout tables.
+// Page citations are in layout.cu.
+#pragma once
+
+#include <math.h>
+#include <stdint.h>
+
+#include "ffmath.cuh"
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Lanes of the warp holding the same expert id as this lane (valid ids >= 0),
+// from one ballot per bit of the id: the bit-plane form of a warp multisplit
+// (Ashkiani et al., "GPU Multisplit", PPoPP 2016). Undefined for e < 0.
+__device__ __forceinline__ unsigned peer_mask(int e, int nbits) {
+  unsigned m = __ballot_sync(kFull, e >= 0);
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned bb = __ballot_sync(kFull, bit);
+    m &= bit ? bb : ~bb;
+  }
+  return m;
+}
+
+// Exclusive scan in place of a[0..n) held in shared memory, by the whole CTA.
+// tmp: 32 ints of shared scratch. Returns the total. Ends with __syncthreads.
+__device__ int cta_exclusive_scan(int* a, int n, int* tmp) {
+  const int nt = blockDim.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = (n + nt - 1) / nt;
+  const int b0 = min(n, (int)threadIdx.x * per), b1 = min(n, b0 + per);
+  int local = 0;
+  for (int i = b0; i < b1; ++i) local += a[i];
+  int v = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int u = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += u;
+  }
+  if (lane == 31) tmp[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nt >> 5;
+    int x = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int u = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += u;
+    }
+    tmp[lane] = x;
+  }
+  __syncthreads();
+  int run = v - local + (warp > 0 ? tmp[warp - 1] : 0);
+  const int total = tmp[(nt >> 5) - 1];
+  for (int i = b0; i < b1; ++i) {
+    int t = a[i];
+    a[i] = run;
+    run += t;
+  }
+  __syncthreads();
+  return total;
+}
+
+// Order-preserving map of a finite float to an unsigned key (larger float ->
+// larger key); -0 is mapped like +0 so that equal logits tie. Key 0 is below
+// every finite float and marks an empty or already chosen register.
+__device__ __forceinline__ unsigned order_key(float v) {
+  const unsigned u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Top-k of one token by one warp: k rounds of a warp-wide arg-max (larger
+// logit first, lower expert index on ties), each round one max-reduction of
+// the keys and one min-reduction of the tied candidates' expert indices.
+// Register i of a lane holds expert i*32 + lane. Lane j < k returns slot j.
+template <int EPL>
+__device__ __forceinline__ void load_keys(const float* __restrict__ z, int E, int lane,
+                                          unsigned (&key)[EPL]) {
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = i * 32 + lane;
+    key[i] = e < E ? order_key(__ldg(z + e)) : 0u;
+  }
+}
+
+template <int EPL>
+__device__ __forceinline__ void topk_select(unsigned (&key)[EPL], int k, int lane, int& out_id,
+                                            float& out_z) {
+  out_id = -1;
+  out_z = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    unsigned bk = 0u;
+    unsigned bi = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (key[i] > bk) {  // strict: the lowest register (expert) wins a tie in a lane
+        bk = key[i];
+        bi = (unsigned)(i * 32 + lane);
+      }
+    }
+    const unsigned m = __reduce_max_sync(kFull, bk);
+    const unsigned win = __reduce_min_sync(kFull, bk == m ? bi : 0xffffffffu);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (win == (unsigned)(i * 32 + lane)) key[i] = 0u;
+    if (lane == j) {
+      out_id = (int)win;
+      out_z = key_value(m);
+    }
+  }
+}
+
+__device__ __forceinline__ float pow2f(int n) {  // 2^n for -126 <= n <= 127
+  return __uint_as_float((unsigned)(n + 127) << 23);
+}
+
+// Routes up to G = 32/K2 consecutive tokens with one warp (K2 = k rounded up
+// to a power of two): selects each token's top-k, then evaluates all their
+// softmax weights at once, token t's slot j on lane t*K2 + j. Weights are
+// w_j = exp(z_j - z_0) / sum_i exp(z_i - z_0) in float-float arithmetic (see
+// ffmath.cuh), rounded once to fp32; the sum is a butterfly inside the lane
+// group (its order does not matter at this precision).
+// Returns, per lane, its token (lane / K2), slot (lane % K2), id and weight;
+// valid is false for lanes past the token count or the top-k.
+template <int EPL>
+__device__ __forceinline__ void route_group_warp(const float* __restrict__ logits, long long g0,
+                                                 int ntok, int E, int k, int K2, int lane,
+                                                 bool& valid, int& id, float& w) {
+  const int grp = lane / K2, slot = lane - grp * K2;
+  valid = grp < ntok && slot < k;
+  id = -1;
+  float my_z = 0.0f;
+  // The logits of up to kPre tokens are loaded before any is selected.
+  constexpr int kPre = EPL >= 32 ? 1 : (32 / EPL < 4 ? 32 / EPL : 4);
+  for (int t0 = 0; t0 < ntok; t0 += kPre) {
+    unsigned key[kPre][EPL];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u)
+      if (t0 + u < ntok) load_keys<EPL>(logits + (g0 + t0 + u) * (long long)E, E, lane, key[u]);
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      if (t0 + u < ntok) {
+        int tid_;
+        float tz;
+        topk_select<EPL>(key[u], k, lane, tid_, tz);
+        const int sid = __shfl_sync(kFull, tid_, slot);
+        const float sz = __shfl_sync(kFull, tz, slot);
+        if (grp == t0 + u) {
+          id = sid;
+          my_z = sz;
+        }
+      }
+    }
+  }
+  const float z0 = __shfl_sync(kFull, my_z, lane & ~(K2 - 1));
+  const ff::F2 d = valid ? ff::two_sum(my_z, -z0) : ff::F2{0.0f, 0.0f};  // exact, <= 0
+  const bool tiny = d.hi < -80.0f;  // exp(d) < 2^-115: evaluated separately below
+  int n = 0;
+  const ff::F2 m = ff::exp_reduced(tiny ? ff::F2{0.0f, 0.0f} : d, n);
+  const float sc = pow2f(n);
+  ff::F2 sum = (valid && !tiny) ? ff::F2{__fmul_rn(m.hi, sc), __fmul_rn(m.lo, sc)}
+                                : ff::F2{0.0f, 0.0f};
+  for (int o = K2 >> 1; o > 0; o >>= 1) {
+    const ff::F2 other{__shfl_xor_sync(kFull, sum.hi, o), __shfl_xor_sync(kFull, sum.lo, o)};
+    sum = ff::add(sum, other);
+  }
+  if (!tiny) {
+    const ff::F2 q = ff::div(m, sum);
+    w = __fmul_rn(__fadd_rn(q.hi, q.lo), sc);
+  } else {
+    // logit gap above 80 inside the top-k: a weight below 2^-115, in double
+    w = (float)(exp((double)my_z - (double)z0) / ((double)sum.hi + (double)sum.lo));
+  }
+}
+
+// The layout tables, by the last CTA of the scan kernel: reads n_kept,
+// n_raw and the per-(source, expert) prefixes into shared memory, scans the
+// kept counts in global expert order (expert offsets) and derives every
+// per-(source, expert) and per-(source, rank) table and the totals.
+__device__ void layout_tables(const LayoutArgs& p, int* smem) {
+  const int E = p.E, P = p.P, tid = threadIdx.x, NT = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int* sk = smem;                   // [E]        kept counts -> expert offsets
+  int* sraw = sk + E;               // [E]
+  int* pre = sraw + E;              // [(P+1)*E]  prefix at each source's first chunk
+  int* Cs = pre + (P + 1) * E;      // [P*P]      count matrix
+  int* tmp = Cs + P * P;            // [32]
+  int* red = tmp + 32;              // [2]        dropped, raw total
+  if (tid < 2) red[tid] = 0;
+  for (int e = tid; e < E; e += NT) {
+    sk[e] = __ldcg(p.n_kept + e);
+    sraw[e] = __ldcg(p.n_raw + e);
+  }
+  for (int i = tid; i < (P + 1) * E; i += NT) pre[i] = __ldcg(p.src_pre + i);
+  __syncthreads();
+  {
+    int dr = 0, rw = 0;
+    for (int e = tid; e < E; e += NT) {
+      rw += sraw[e];
+      dr += sraw[e] - sk[e];
+    }
+    if (dr) atomicAdd(&red[0], dr);
+    if (rw) atomicAdd(&red[1], rw);
+  }
+  // Expert offsets: exclusive scan of kept counts in global expert order.
+  const int total = cta_exclusive_scan(sk, E, tmp);
+  for (int e = tid; e <= E; e += NT) p.expert_offset[e] = e < E ? sk[e] : total;
+  for (int d = tid; d <= P; d += NT) p.rank_base[d] = d < P ? sk[d * p.L] : total;
+  auto kept_of = [&](int s, int e) {
+    const int a = pre[s * E + e];
+    const int c = pre[(s + 1) * E + e] - a;
+    return p.cap > 0 ? min(max(p.cap - a, 0), c) : c;
+  };
+  // Per (source, expert): raw and kept counts, receive offsets.
+  for (int it = tid; it < P * E; it += NT) {
+    const int s = it / E, e = it - s * E;
+    const int a = pre[s * E + e];
+    p.cnt[it] = pre[(s + 1) * E + e] - a;
+    p.kept_cnt[it] = kept_of(s, e);
+    p.recv_offset[it] = sk[e] + (p.cap > 0 ? min(a, p.cap) : a);
+  }
+  // Count matrix C[s][d] = kept assignments of source s to the experts of d:
+  // one thread per (s, d) for few local experts, one warp per (s, d) for many.
+  if (p.L < 16) {
+    for (int it = tid; it < P * P; it += NT) {
+      const int s = it / P, d = it - s * P;
+      int sum = 0;
+      for (int e = d * p.L; e < (d + 1) * p.L; ++e) sum += kept_of(s, e);
+      Cs[it] = sum;
+      p.C[it] = sum;
+    }
+  } else {
+    for (int it = warp; it < P * P; it += NT / 32) {
+      const int s = it / P, d = it - s * P;
+      int sum = 0;
+      for (int e = d * p.L + lane; e < (d + 1) * p.L; e += 32) sum += kept_of(s, e);
+      sum = __reduce_add_sync(kFull, sum);
+      if (lane == 0) {
+        Cs[it] = sum;
+        p.C[it] = sum;
+      }
+    }
+  }
+  __syncthreads();
+  // Send offsets: exclusive prefix of C[s][.] over destinations, one warp per s.
+  for (int s = warp; s < P; s += NT / 32) {
+    int carry = 0;
+    for (int d0 = 0; d0 < P; d0 += 32) {
+      const int d = d0 + lane;
+      const int v = d < P ? Cs[s * P + d] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      if (d < P) p.send_offset[(long long)s * P + d] = carry + x - v;
+      carry += __shfl_sync(kFull, x, 31);
+    }
+  }
+  if (tid == 0) {
+    p.totals[0] = total;
+    p.totals[1] = red[0];
+    p.totals[2] = (int)(p.Na - (long long)red[1]);
+    p.totals[3] = 0;
+    *p.done = 0u;  // ready for the next layout on this workspace
+  }
+}
+
+// One chunk (CTA b): route its tokens or load their ids, count them per warp,
+// write the chunk's per-expert counts into the transposed table
+// hist[e * nchunks + b], and give every assignment its stable chunk-local rank
+// (assignment code). Shared memory: wcnt[kLayoutWarps][E], ids_s[tpc*k].
+template <bool ROUTE, int EPL>
+__device__ __forceinline__ void layout_chunk(const LayoutArgs& p, int b, int* smem) {
+  const int E = p.E;
+  int* wcnt = smem;                                         // [warps][E]
+  const int wcnt_ints = kLayoutWarps * E;
+  int* ids_s = smem + wcnt_ints;                            // [tpc*k]
+
+  const int s = b / p.cps, c = b - s * p.cps;
+  const int t0 = c * p.tpc;
+  const int nt = min(p.tpc, p.Tr - t0);
+  const long long g0 = (long long)s * p.Tr + t0;
+  const long long a0 = g0 * p.k;
+  const int na = nt * p.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int i = tid; i < wcnt_ints; i += kLayoutThreads) wcnt[i] = 0;
+  pdl_wait();  // logits / ids may come from the previous kernel
+  pdl_trigger();
+
+  if (ROUTE) {
+    int K2 = 1;
+    while (K2 < p.k) K2 <<= 1;
+    // tokens routed together by one warp: one when the chunk is small (latency),
+    // up to 32/K2 when there are many (fewer instructions per token)
+    const int G = min(32 / K2, (nt + kLayoutWarps - 1) / kLayoutWarps);
+    for (int tl0 = warp * G; tl0 < nt; tl0 += kLayoutWarps * G) {
+      bool valid;
+      int id;
+      float wt;
+      route_group_warp<EPL>(p.logits, g0 + tl0, min(G, nt - tl0), E, p.k, K2, lane, valid, id, wt);
+      if (valid) {
+        const int tl = tl0 + lane / K2, j = lane % K2;
+        ids_s[tl * p.k + j] = id;
+        p.ids_out[(g0 + tl) * p.k + j] = id;
+        p.w_out[(g0 + tl) * p.k + j] = wt;
+      }
+    }
+  } else {
+    for (int i = tid; i < na; i += kLayoutThreads) {
+      int e = __ldg(p.ids_in + a0 + i);
+      if (e < -1 || e >= E) {
+        atomicOr(p.status, MOE_STATUS_BAD_EXPERT_ID);
+        e = -1;
+      }
+      ids_s[i] = e;
+    }
+  }
+  __syncthreads();
+
+  // Pass 1: per-warp expert counts of the warp's contiguous sub-range.
+  const int per = (na + kLayoutWarps - 1) / kLayoutWarps;
+  const int beg = min(na, warp * per), end = min(na, beg + per);
+  int nbits = 0;
+  while ((1 << nbits) < E) ++nbits;
+  for (int base = beg; base < end; base += 32) {
+    const int i = base + lane;
+    const int e = i < end ? ids_s[i] : -1;
+    const unsigned m = peer_mask(e, nbits);
+    if (e >= 0 && lane == __ffs(m) - 1) wcnt[warp * E + e] += __popc(m);
+  }
+  __syncthreads();
+  // Per-expert exclusive scan over warps; the chunk's histogram row.
+  for (int e = tid; e < E; e += kLayoutThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kLayoutWarps; ++w) {
+      const int v = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += v;
+    }
+    p.hist[(long long)e * p.nchunks + b] = run;  // transposed: [E][nchunks]
+  }
+  __syncthreads();
+  // Pass 2: stable rank of every assignment within the chunk and expert.
+  const unsigned below = (1u << lane) - 1u;
+  for (int base = beg; base < end; base += 32) {
+    const int i = base + lane;
+    const int e = i < end ? ids_s[i] : -1;
+    const unsigned m = peer_mask(e, nbits);
+    int code = -1;
+    if (e >= 0) code = (e << 16) | (wcnt[warp * E + e] + __popc(m & below));
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(m) - 1) wcnt[warp * E + e] += __popc(m);
+    __syncwarp();
+    if (i < end) p.acode[a0 + i] = code;
+  }
+
+}
+
+}  // namespace
+}  // namespace moe

@@ -65,6 +65,13 @@ class MoeLayer:
         B.moe_dispatch_two_stage(self.handle, x, w, self.send_x, self.send_scale, self.recv_x,
                                  self.recv_scale, self.meta, stream)
 
+    def layout_dispatch_fused(self, x, ids=None, w=None, logits=None, stream=None):
+        """One persistent launch: route (logits) or take ids/w, lay out, dispatch."""
+        if logits is not None:
+            ids, w = self.ids, self.w
+        B.moe_layout_dispatch_fused(self.handle, logits, ids, w, x, self.recv_x, self.recv_scale,
+                                    self.meta, stream)
+
     def expert(self, expert_scale=None, stream=None):
         B.moe_expert_standin(self.handle, self.recv_x, self.recv_scale, expert_scale, self.y,
                              stream)
@@ -73,9 +80,16 @@ class MoeLayer:
         B.moe_combine(self.handle, self.y, w, self.out, stream)
 
     def forward(self, x, ids=None, w=None, logits=None, expert_scale=None, stream=None,
-                two_stage=False):
+                two_stage=False, fused=False):
         """Whole layer; with logits the routed ids/weights land in self.ids / self.w.
         two_stage=True dispatches through the two-stage comparator."""
+        if fused:
+            self.layout_dispatch_fused(x, ids, w, logits, stream)
+            if logits is not None:
+                w = self.w
+            self.expert(expert_scale, stream)
+            self.combine(w, stream)
+            return self.out
         if logits is not None:
             self.route_layout(logits, stream)
             w = self.w

@@ -199,6 +199,29 @@ int moe_get_layout(moe_handle_t h, moe_layout_view_t *out);
 int moe_dispatch(moe_handle_t h, const void *x, const float *w, void *recv_x,
                  float *recv_scale, const moe_recv_meta_t *meta, void *stream);
 
+/* Persistent single-launch path for small, latency-bound layers (decode):
+ * route (logits != NULL: ids and w are written, as moe_route_dispatch_layout)
+ * or take given ids and w (logits == NULL), build the layout and dispatch the
+ * payload -- everything moe_[route_]dispatch_layout + moe_dispatch produce,
+ * bit for bit -- in ONE cooperative launch with one CTA per SM ([A2A] 9-10:
+ * a low-latency mode with persistent kernels and device-side
+ * synchronisation). Each CTA owns a chunk of one source rank's tokens and
+ * streams their x rows into shared memory while it routes and counts; two
+ * grid barriers separate counting, the column scans and the scatter. Every
+ * barrier gives up after the handle's wait limit (moe_set_wait_limit), sets
+ * MOE_STATUS_TIMEOUT and leaves the kernel; the outputs of such a call are
+ * undefined and the next call works normally.
+ * Returns MOE_ERR_UNSUPPORTED (enqueuing nothing) when one chunk per SM would
+ * hold more than 4096 assignments, when P exceeds the SM count, or when the
+ * cooperative grid cannot be resident; use the separate calls then. */
+int moe_layout_dispatch_fused(moe_handle_t h, const float *logits, int32_t *ids, float *w,
+                              const void *x, void *recv_x, float *recv_scale,
+                              const moe_recv_meta_t *meta, void *stream);
+
+/* Polls a bounded device wait makes before giving up (default 2^22, about
+ * 0.3 s). 0 makes every wait give up at once: for testing the timeout path. */
+int moe_set_wait_limit(moe_handle_t h, int64_t polls);
+
 /* NEXT-row comparator, the "standard" two-stage dispatch ([A2A] 4.3 and 5.2):
  * stage 1 packs every kept assignment into its source rank's send buffer
  * ([to rank 0][to rank 1]..., each destination segment bucketed by local
