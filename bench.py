@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--dispatch", default="separate", choices=["separate", "fused", "two_stage"],
                     help="separate: layout kernels then the dispatch kernel; fused: one "
                          "persistent launch; two_stage: the pack + all-to-all-v comparator")
+    ap.add_argument("--pipeline", type=int, default=0,
+                    help="also time the token-chunked two-stream pipeline with N chunks")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="override T_r (a smaller case of the same workload, e.g. for ncu)")
     return ap.parse_args()
@@ -329,13 +331,14 @@ def run_ours(args, wl, rank, world, local):
         dispatch()
         ev[2].record(stream)
         layer.expert(c, stream)
+        ev[5].record(stream)
         flush_l2()
         ev[3].record(stream)
         layer.combine(w, stream)
         ev[4].record(stream)
 
     def new_events(n):
-        return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n)]
 
     for ev in new_events(args.warmup):
         step(ev)
@@ -362,6 +365,32 @@ def run_ours(args, wl, rank, world, local):
     lay_ms = [e[0].elapsed_time(e[1]) for e in devs]
     dis_ms = [e[1].elapsed_time(e[2]) for e in devs]
     com_ms = [e[3].elapsed_time(e[4]) for e in devs]
+    exp_ms = [e[2].elapsed_time(e[5]) for e in devs]
+
+    pipeline = None
+    if args.pipeline > 0 and args.dispatch == "separate":
+        # token-chunked two-stream pipeline, the whole layer incl. the expert
+        # stand-in, against the sum of the same stages run one after another
+        pevs = new_events(min(args.steps, 50) + 3)
+        for i, ev in enumerate(pevs):
+            flush_l2()
+            ev[0].record(stream)
+            if routed:
+                layer.forward_pipelined(x, logits=logits, expert_scale=c, chunks=args.pipeline,
+                                        stream=stream)
+            else:
+                layer.forward_pipelined(x, ids=ids, w=w, expert_scale=c, chunks=args.pipeline,
+                                        stream=stream)
+            ev[1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = statistics.fmean([e[0].elapsed_time(e[1]) for e in pevs[3:]])
+        stages = statistics.fmean([a + b + x_ + d for a, b, x_, d in
+                                   zip(lay_ms, dis_ms, exp_ms, com_ms)])
+        pipeline = {"chunks": args.pipeline, "wall_us": round(wall * 1e3, 3),
+                    "sum_stages_us": round(stages * 1e3, 3),
+                    "sum_over_wall": round(stages / wall, 4),
+                    "note": "whole layer incl. the expert stand-in; stages timed serially "
+                            "with L2 flushed only before layout and combine"}
 
     # warm: no flushes (a layer right after the previous one; L2 keeps what fits)
     wevs = new_events(min(args.steps, 100))
@@ -404,7 +433,24 @@ def run_ours(args, wl, rank, world, local):
         e2e_ms.append(ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]))
     e2e_us = max_over_ranks(statistics.fmean(e2e_ms) * 1e3, world)
 
-    kept = int(layer.layout_view()["totals"][0].item())
+    view = layer.layout_view()
+    kept = int(view["totals"][0].item())
+    # routing shape ("Expert Parallel: MoE Token ...", "Load skew amplifies
+    # both compute and communication tails" and "What to record"): expert
+    # imbalance I_e = max n_e / mean n_e, rank imbalance I_r = max L_r / mean,
+    # local fraction = kept assignments whose expert lives on their source rank
+    n_e = view["expert_count"].double().cpu()
+    Cm = view["count_matrix"].double().cpu()
+    load_r = Cm.sum(dim=0)
+    routing_shape = {
+        "I_e": round(float(n_e.max() / n_e.mean()), 4) if float(n_e.mean()) > 0 else None,
+        "I_r": round(float(load_r.max() / load_r.mean()), 4) if float(load_r.mean()) > 0 else None,
+        "local_fraction": round(float(Cm.diagonal().sum() / Cm.sum()), 4) if float(Cm.sum()) > 0 else None,
+        "kept": kept, "dropped": int(view["totals"][1].item()),
+        "masked": int(view["totals"][2].item()),
+        "C_row_sums": [int(v) for v in Cm.sum(dim=1).tolist()],
+        "C_col_sums": [int(v) for v in load_r.tolist()],
+    }
     kb = accounting.hbm_bytes(wl.P, wl.Tr, wl.E, wl.k, wl.H, layer.fp8, rows=kept, routed=routed)
     pay = accounting.payload_bytes(wl.P, wl.Tr, wl.k, wl.H, layer.fp8, rows=kept)
     dkey = "k_dispatch_fp8" if layer.fp8 else "k_dispatch_bf16"
@@ -457,6 +503,9 @@ def run_ours(args, wl, rank, world, local):
         "payload_gbs": round(pay["total"] / (mean_ms_all * 1e-3) / 1e9, 1),
         "warm_us_per_layer": round(warm_ms * 1e3, 3),
         "kept_rows": kept,
+        "routing": routing_shape,
+        "pipeline": pipeline,
+        "host_cores": os.cpu_count(),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "moe_dispatch", "moe_expert_standin", "moe_combine", "moe_read_status", "moe_error_string",
     "moe_dispatch_layout_noalloc", "moe_copy_h2d_async", "moe_copy_d2h_async",
     "moe_dispatch_two_stage", "moe_layout_dispatch_fused", "moe_set_wait_limit",
+    "moe_dispatch_tokens", "moe_expert_standin_tokens", "moe_combine_tokens",
 )
 
 
@@ -107,6 +108,14 @@ def load_library():
                                                   ctypes.POINTER(moe_recv_meta_t), vp]
         lib.moe_set_wait_limit.restype = i32
         lib.moe_set_wait_limit.argtypes = [vp, ctypes.c_int64]
+        i64 = ctypes.c_int64
+        lib.moe_dispatch_tokens.restype = i32
+        lib.moe_dispatch_tokens.argtypes = [vp, i64, i64, vp, vp, vp, vp,
+                                            ctypes.POINTER(moe_recv_meta_t), vp]
+        lib.moe_expert_standin_tokens.restype = i32
+        lib.moe_expert_standin_tokens.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp]
+        lib.moe_combine_tokens.restype = i32
+        lib.moe_combine_tokens.argtypes = [vp, i64, i64, vp, vp, vp, vp]
         lib.moe_expert_standin.restype = i32
         lib.moe_expert_standin.argtypes = [vp, vp, vp, vp, vp, vp]
         lib.moe_combine.restype = i32
@@ -269,6 +278,27 @@ def moe_layout_dispatch_fused(h: Handle, logits, ids, w, x, recv_x, recv_scale, 
 
 def moe_set_wait_limit(h: Handle, polls: int) -> None:
     _check("moe_set_wait_limit", load_library().moe_set_wait_limit(h.ptr, int(polls)))
+
+
+def moe_dispatch_tokens(h: Handle, begin: int, end: int, x, w, recv_x, recv_scale, meta: dict,
+                        stream=None) -> None:
+    m = moe_recv_meta_t(*(_ptr(meta[n]) for n in (
+        "local_expert", "src_rank", "src_token", "slot", "weight")))
+    _check("moe_dispatch_tokens", load_library().moe_dispatch_tokens(
+        h.ptr, int(begin), int(end), _ptr(x), _ptr(w), _ptr(recv_x), _ptr(recv_scale),
+        ctypes.byref(m), _stream(stream)))
+
+
+def moe_expert_standin_tokens(h: Handle, begin: int, end: int, recv_x, recv_scale, expert_scale,
+                              y, stream=None) -> None:
+    _check("moe_expert_standin_tokens", load_library().moe_expert_standin_tokens(
+        h.ptr, int(begin), int(end), _ptr(recv_x), _ptr(recv_scale), _ptr(expert_scale),
+        _ptr(y), _stream(stream)))
+
+
+def moe_combine_tokens(h: Handle, begin: int, end: int, y, w, out, stream=None) -> None:
+    _check("moe_combine_tokens", load_library().moe_combine_tokens(
+        h.ptr, int(begin), int(end), _ptr(y), _ptr(w), _ptr(out), _stream(stream)))
 
 
 def moe_expert_standin(h: Handle, recv_x, recv_scale, expert_scale, y, stream=None) -> None:

@@ -276,8 +276,9 @@ int moe_get_layout(moe_handle_t h, moe_layout_view_t* out) {
   return MOE_OK;
 }
 
-int moe_dispatch(moe_handle_t h, const void* x, const float* w, void* recv_x, float* recv_scale,
-                 const moe_recv_meta_t* meta, void* stream) {
+static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void* x,
+                          const float* w, void* recv_x, float* recv_scale,
+                          const moe_recv_meta_t* meta, void* stream) {
   if (!h || !x || !w || !recv_x || !meta) return MOE_ERR_INVALID_ARG;
   if (!meta->local_expert || !meta->src_rank || !meta->src_token || !meta->slot || !meta->weight)
     return MOE_ERR_INVALID_ARG;
@@ -299,7 +300,8 @@ int moe_dispatch(moe_handle_t h, const void* x, const float* w, void* recv_x, fl
   a.m_src_token = meta->src_token;
   a.m_slot = meta->slot;
   a.m_weight = meta->weight;
-  a.T = h->T;
+  a.T = g1;
+  a.g0 = g0;
   a.Tr = h->cfg.tokens_per_rank;
   a.k = h->cfg.top_k;
   a.E = h->cfg.num_experts;
@@ -374,6 +376,20 @@ int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* 
   rc = cuda_rc(moe::launch_a2av(c, h->num_sms, st));
   if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
   return rc;
+}
+
+int moe_dispatch(moe_handle_t h, const void* x, const float* w, void* recv_x, float* recv_scale,
+                 const moe_recv_meta_t* meta, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  return dispatch_range(h, 0, h->T, x, w, recv_x, recv_scale, meta, stream);
+}
+
+int moe_dispatch_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end, const void* x,
+                        const float* w, void* recv_x, float* recv_scale,
+                        const moe_recv_meta_t* meta, void* stream) {
+  if (!h || token_begin < 0 || token_end > h->T || token_begin > token_end)
+    return MOE_ERR_INVALID_ARG;
+  return dispatch_range(h, token_begin, token_end, x, w, recv_x, recv_scale, meta, stream);
 }
 
 int moe_set_wait_limit(moe_handle_t h, int64_t polls) {
@@ -476,7 +492,8 @@ int moe_expert_standin(moe_handle_t h, const void* recv_x, const float* recv_sca
   return cuda_rc(moe::launch_standin(a, h->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
-int moe_combine(moe_handle_t h, const void* y, const float* w, void* out, void* stream) {
+static int combine_range(moe_handle_t h, long long g0, long long g1, const void* y, const float* w,
+                         void* out, void* stream) {
   if (!h || !y || !w || !out) return MOE_ERR_INVALID_ARG;
   if (!aligned(y, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   if (h->dispatch_gen == 0 || h->dispatch_gen != h->layout_gen) return MOE_ERR_STATE;
@@ -485,10 +502,49 @@ int moe_combine(moe_handle_t h, const void* y, const float* w, void* out, void* 
   a.w = w;
   a.inv = h->inv;
   a.out = static_cast<uint16_t*>(out);
-  a.T = h->T;
+  a.T = g1;
+  a.g0 = g0;
   a.k = h->cfg.top_k;
   a.H = h->cfg.hidden;
   return cuda_rc(moe::launch_combine(a, h->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_combine(moe_handle_t h, const void* y, const float* w, void* out, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  return combine_range(h, 0, h->T, y, w, out, stream);
+}
+
+int moe_combine_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end, const void* y,
+                       const float* w, void* out, void* stream) {
+  if (!h || token_begin < 0 || token_end > h->T || token_begin > token_end)
+    return MOE_ERR_INVALID_ARG;
+  return combine_range(h, token_begin, token_end, y, w, out, stream);
+}
+
+int moe_expert_standin_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end,
+                              const void* recv_x, const float* recv_scale,
+                              const float* expert_scale, void* y, void* stream) {
+  if (!h || !recv_x || !y || token_begin < 0 || token_end > h->T || token_begin > token_end)
+    return MOE_ERR_INVALID_ARG;
+  const bool fp8 = h->cfg.dispatch_dtype == MOE_FP8_E4M3;
+  if (fp8 && !recv_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned(recv_x, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  if (h->dispatch_gen == 0 || h->dispatch_gen != h->layout_gen) return MOE_ERR_STATE;
+  moe::StandinArgs a{};
+  a.inv = h->inv;
+  a.a0 = token_begin * h->cfg.top_k;
+  a.a1 = token_end * h->cfg.top_k;
+  a.k = h->cfg.top_k;
+  a.recv = recv_x;
+  a.recv_scale = recv_scale;
+  a.expert_scale = expert_scale;
+  a.expert_offset = h->expert_offset;
+  a.y = static_cast<uint16_t*>(y);
+  a.rows_max = h->rows_max;
+  a.E = h->cfg.num_experts;
+  a.H = h->cfg.hidden;
+  a.fp8 = fp8 ? 1 : 0;
+  return cuda_rc(moe::launch_standin_tokens(a, h->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_read_status(moe_handle_t h, uint32_t* flags, void* stream) {

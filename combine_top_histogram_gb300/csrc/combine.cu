@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const CombineArgs p
   const int k = K > 0 ? K : p.k;
   pdl_wait();  // y (and inv, when dispatch ran just before) come from earlier kernels
   pdl_trigger();
-  for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
+  for (long long g = p.g0 + blockIdx.x; g < p.T; g += gridDim.x) {
     if (tid < k) {
       rows_s[tid] = __ldg(p.inv + g * k + tid);
       w_s[tid] = __ldg(p.w + g * k + tid);
@@ -174,11 +174,79 @@ __global__ void __launch_bounds__(128) k_standin(const StandinArgs p) {
   }
 }
 
+// Token-range stand-in: the rows of assignments [a0, a1) (a token chunk's
+// slots), found through inv; same per-row function as k_standin.
+__global__ void __launch_bounds__(128) k_standin_tokens(const StandinArgs p) {
+  __shared__ float c_s;
+  __shared__ int r_s;
+  const int nvec = p.H >> 3;
+  pdl_wait();
+  pdl_trigger();
+  for (long long a = p.a0 + blockIdx.x; a < p.a1; a += gridDim.x) {
+    if (threadIdx.x == 0) {
+      const int r = __ldg(p.inv + a);
+      r_s = r;
+      if (r >= 0) {
+        int lo = 0, hi = p.E - 1;  // largest e with expert_offset[e] <= r
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (__ldg(p.expert_offset + mid) <= r) lo = mid;
+          else hi = mid - 1;
+        }
+        c_s = p.expert_scale ? __ldg(p.expert_scale + lo) : 1.0f;
+      }
+    }
+    __syncthreads();
+    const long long r = r_s;
+    if (r >= 0) {
+      const float c = c_s;
+      uint4* dst = reinterpret_cast<uint4*>(p.y + r * p.H);
+      for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+        float f[8];
+        if (p.fp8) {
+          const uint2 q = reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(p.recv) + r * p.H)[v];
+          const float s = __ldg(p.recv_scale + r * (p.H >> 7) + (v >> 4));
+          const uint32_t qq[2] = {q.x, q.y};
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const __nv_fp8_storage_t byte = (__nv_fp8_storage_t)((qq[b >> 2] >> (8 * (b & 3))) & 0xffu);
+            const __half_raw hr = __nv_cvt_fp8_to_halfraw(byte, __NV_E4M3);
+            f[b] = __fmul_rn(c, __fmul_rn(__half2float(__half(hr)), s));
+          }
+        } else {
+          const uint4 x = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.recv) + r * p.H)[v];
+          const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            f[2 * q] = __fmul_rn(c, bf16_lo(u[q]));
+            f[2 * q + 1] = __fmul_rn(c, bf16_hi(u[q]));
+          }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(f[0], f[1]);
+        o.y = pack_bf16x2(f[2], f[3]);
+        o.z = pack_bf16x2(f[4], f[5]);
+        o.w = pack_bf16x2(f[6], f[7]);
+        dst[v] = o;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
+cudaError_t launch_standin_tokens(const StandinArgs& a, int num_sms, cudaStream_t st) {
+  if (a.a1 - a.a0 <= 0) return cudaSuccess;
+  long long blocks = a.a1 - a.a0;
+  const long long cap = (long long)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(k_standin_tokens, dim3((int)blocks), dim3(128), 0, st, a);
+}
+
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st) {
-  if (a.T <= 0) return cudaSuccess;
-  long long blocks = a.T;
+  if (a.T - a.g0 <= 0) return cudaSuccess;
+  long long blocks = a.T - a.g0;
   const long long cap = (long long)num_sms * 16;
   if (blocks > cap) blocks = cap;
   switch (a.k) {

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_bf16(const Dispat
   const int nvec = p.H >> 3;  // 16-byte vectors per row
   const int tid = threadIdx.x;
   bool waited = false;
-  for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
+  for (long long g = p.g0 + blockIdx.x; g < p.T; g += gridDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const Dispatc
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
   bool waited = false;
-  for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
+  for (long long g = p.g0 + blockIdx.x; g < p.T; g += gridDim.x) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -164,8 +164,8 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const Dispatc
 }  // namespace
 
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st) {
-  if (a.T <= 0) return cudaSuccess;
-  long long blocks = a.T;
+  if (a.T - a.g0 <= 0) return cudaSuccess;
+  long long blocks = a.T - a.g0;
   const long long cap = (long long)num_sms * 16;  // 16 CTAs of 128 threads fill an SM
   if (blocks > cap) blocks = cap;
   const int nvec = a.H >> 3;

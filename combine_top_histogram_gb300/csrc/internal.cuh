@@ -69,7 +69,8 @@ struct DispatchArgs {
   int32_t* m_src_token;
   int32_t* m_slot;
   float* m_weight;
-  long long T;
+  long long T;            // tokens [g0, T) are dispatched (g0 = 0: all)
+  long long g0;
   int Tr, k, E, L, H, tpc, cps, nchunks, cap;
   // Two-stage comparator: when send_pos is set, payload rows go to the send
   // pool row src_base[s] + send_pos[s][e] + (r - recv_offset[s][e]) instead of
@@ -108,11 +109,15 @@ struct CombineArgs {
   const float* w;         // [T*k]
   const int32_t* inv;     // [T*k]
   uint16_t* out;          // bf16 [T*H]
-  long long T;
+  long long T;            // tokens [g0, T) are combined (g0 = 0: all)
+  long long g0;
   int k, H;
 };
 
 struct StandinArgs {
+  const int32_t* inv;      // token-range form: rows of assignments [a0, a1)
+  long long a0, a1;
+  int k;
   const void* recv;        // bf16 or e4m3 [rows*H]
   const float* recv_scale; // FP8 scales
   const float* expert_scale; // [E] or null
@@ -160,6 +165,7 @@ cudaError_t layout_prepare(int E, int tpc, int k, int P);
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_standin(const StandinArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_standin_tokens(const StandinArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_send_pos(const int32_t* kept_cnt, int32_t* send_pos, int32_t* src_base, int P,
                             int E, cudaStream_t st);
 cudaError_t launch_a2av(const A2avArgs& a, int num_sms, cudaStream_t st);

@@ -103,6 +103,36 @@ class MoeLayer:
         self.combine(w, stream)
         return self.out
 
+    def forward_pipelined(self, x, ids=None, w=None, logits=None, expert_scale=None, chunks=4,
+                          stream=None):
+        """The layer in token chunks on two streams: after the layout, chunk c+1's
+        dispatch (main stream) overlaps chunk c's expert and combine (side
+        stream, ordered after chunk c's dispatch by an event)."""
+        import torch
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if getattr(self, "_side", None) is None:
+            self._side = torch.cuda.Stream(device=self.out.device)
+        side = self._side
+        if logits is not None:
+            self.route_layout(logits, main)
+            w = self.w
+        else:
+            self.layout(ids, main)
+        side.wait_stream(main)
+        bounds = [self.T * c // chunks for c in range(chunks + 1)]
+        for c in range(chunks):
+            b0, b1 = bounds[c], bounds[c + 1]
+            B.moe_dispatch_tokens(self.handle, b0, b1, x, w, self.recv_x, self.recv_scale,
+                                  self.meta, main)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            side.wait_event(ev)
+            B.moe_expert_standin_tokens(self.handle, b0, b1, self.recv_x, self.recv_scale,
+                                        expert_scale, self.y, side)
+            B.moe_combine_tokens(self.handle, b0, b1, self.y, w, self.out, side)
+        main.wait_stream(side)
+        return self.out
+
     def layout_view(self) -> dict:
         return B.moe_get_layout(self.handle)
 

@@ -288,6 +288,24 @@ int moe_dispatch_layout_noalloc(const moe_config_t *cfg, const int32_t *ids,
 int moe_copy_h2d_async(void *dst_device, const void *src_host, size_t bytes, void *stream);
 int moe_copy_d2h_async(void *dst_host, const void *src_device, size_t bytes, void *stream);
 
+/* ---- token ranges (NEXT-row pipeline) ----------------------------------------
+ * The dispatch, expert stand-in and combine of the global tokens
+ * [token_begin, token_end) only, after a layout of the whole layer. Each
+ * token's k receive rows are written by the dispatch of its own range, so a
+ * caller can pipeline chunks: dispatch chunk c+1 on one stream while another
+ * stream (ordered after chunk c's dispatch by an event) runs chunk c's expert
+ * and combine ([A2A] 7: start the expert as soon as its inputs have arrived;
+ * [EP] "How communication and compute overlap"). Results equal the
+ * whole-layer calls. Errors: INVALID_ARG (range outside [0, T]), STATE. */
+int moe_dispatch_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end, const void *x,
+                        const float *w, void *recv_x, float *recv_scale,
+                        const moe_recv_meta_t *meta, void *stream);
+int moe_expert_standin_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end,
+                              const void *recv_x, const float *recv_scale,
+                              const float *expert_scale, void *y, void *stream);
+int moe_combine_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end, const void *y,
+                       const float *w, void *out, void *stream);
+
 /* Reads and clears the device status word. Synchronises `stream`: tests and
  * debugging only. *flags receives MOE_STATUS_* bits. */
 int moe_read_status(moe_handle_t h, uint32_t *flags, void *stream);

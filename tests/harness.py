@@ -24,7 +24,8 @@ def to_np_bits(t):
 
 
 def run_gpu(wl: W.Workload, inp: W.Inputs, ids=None, layer=None, stream=None,
-            copy_rows: bool = True, two_stage: bool = False, fused: bool = False):
+            copy_rows: bool = True, two_stage: bool = False, fused: bool = False,
+            pipelined: int = 0):
     """The path on the GPU through the C ABI; returns host copies of everything
     (copy_rows=False leaves the row buffers on the device, in res["layer"])."""
     import torch
@@ -34,7 +35,17 @@ def run_gpu(wl: W.Workload, inp: W.Inputs, ids=None, layer=None, stream=None,
         layer = MoeLayer(wl.P, wl.Tr, wl.E, wl.k, wl.H, wl.dispatch_dtype, wl.cap, "cuda:0")
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
     c = torch.from_numpy(inp.expert_scale).to(dev) if inp.expert_scale is not None else None
-    if ids is None and inp.logits is not None:
+    if pipelined:
+        if ids is None and inp.logits is not None:
+            layer.forward_pipelined(x, logits=torch.from_numpy(inp.logits).to(dev), expert_scale=c,
+                                    chunks=pipelined)
+            w_used = layer.w
+        else:
+            ids_np = inp.ids if ids is None else ids
+            w_used = torch.from_numpy(inp.w).to(dev)
+            layer.forward_pipelined(x, ids=torch.from_numpy(np.ascontiguousarray(ids_np, np.int32)).to(dev),
+                                    w=w_used, expert_scale=c, chunks=pipelined)
+    elif ids is None and inp.logits is not None:
         logits = torch.from_numpy(inp.logits).to(dev)
         layer.forward(x, logits=logits, expert_scale=c, stream=stream, two_stage=two_stage,
                       fused=fused)
