@@ -45,9 +45,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--dispatch", default="separate", choices=["separate", "fused", "two_stage"],
+    ap.add_argument("--dispatch", default="separate",
+                    choices=["separate", "fused", "two_stage", "allgather"],
                     help="separate: layout kernels then the dispatch kernel; fused: one "
-                         "persistent launch; two_stage: the pack + all-to-all-v comparator")
+                         "persistent launch; two_stage: the pack + all-to-all-v comparator; "
+                         "allgather: the all-tokens-to-every-rank comparator")
     ap.add_argument("--pipeline", type=int, default=0,
                     help="also time the token-chunked two-stream pipeline with N chunks")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
@@ -296,6 +298,8 @@ def run_ours(args, wl, rank, world, local):
     def dispatch():
         if args.dispatch == "two_stage":
             layer.dispatch_two_stage(x, w, stream)
+        elif args.dispatch == "allgather":
+            layer.dispatch_allgather(x, w, stream)
         elif args.dispatch == "separate":
             layer.dispatch(x, w, stream)
 
@@ -457,6 +461,8 @@ def run_ours(args, wl, rank, world, local):
     lkey = "k_layout+k_scan"
     if args.dispatch == "two_stage":
         dkey = "two_stage(k_send_pos+" + dkey + "+k_a2av)"
+    if args.dispatch == "allgather":
+        dkey = "allgather(k_allgather+k_allgather_filter)"
     if args.dispatch == "fused":
         lkey = "k_fused(route+layout+dispatch)"
         means = {lkey: statistics.fmean([a + b for a, b in zip(lay_ms, dis_ms)]),
@@ -494,8 +500,8 @@ def run_ours(args, wl, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": (2 if args.dispatch == "fused" else
-                         6 if args.dispatch == "two_stage" else 4) * args.steps,
+        "gpu_launches": (2 if args.dispatch == "fused" else 6 if args.dispatch == "two_stage"
+                         else 5 if args.dispatch == "allgather" else 4) * args.steps,
         "clocks": clk.summary(),
         "per_kernel_us": {k: round(v * 1e3, 3) for k, v in means.items()},
         "assignments_per_s": round(world * wl.Na / (mean_ms_all * 1e-3), 1),

@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "moe_dispatch_layout_noalloc", "moe_copy_h2d_async", "moe_copy_d2h_async",
     "moe_dispatch_two_stage", "moe_layout_dispatch_fused", "moe_set_wait_limit",
     "moe_dispatch_tokens", "moe_expert_standin_tokens", "moe_combine_tokens",
+    "moe_dispatch_allgather",
 )
 
 
@@ -116,6 +117,9 @@ def load_library():
         lib.moe_expert_standin_tokens.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp]
         lib.moe_combine_tokens.restype = i32
         lib.moe_combine_tokens.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+        lib.moe_dispatch_allgather.restype = i32
+        lib.moe_dispatch_allgather.argtypes = [vp, vp, vp, vp, vp, vp, vp,
+                                               ctypes.POINTER(moe_recv_meta_t), vp]
         lib.moe_expert_standin.restype = i32
         lib.moe_expert_standin.argtypes = [vp, vp, vp, vp, vp, vp]
         lib.moe_combine.restype = i32
@@ -299,6 +303,15 @@ def moe_expert_standin_tokens(h: Handle, begin: int, end: int, recv_x, recv_scal
 def moe_combine_tokens(h: Handle, begin: int, end: int, y, w, out, stream=None) -> None:
     _check("moe_combine_tokens", load_library().moe_combine_tokens(
         h.ptr, int(begin), int(end), _ptr(y), _ptr(w), _ptr(out), _stream(stream)))
+
+
+def moe_dispatch_allgather(h: Handle, x, w, gathered_x, gathered_scale, recv_x, recv_scale,
+                           meta: dict, stream=None) -> None:
+    m = moe_recv_meta_t(*(_ptr(meta[n]) for n in (
+        "local_expert", "src_rank", "src_token", "slot", "weight")))
+    _check("moe_dispatch_allgather", load_library().moe_dispatch_allgather(
+        h.ptr, _ptr(x), _ptr(w), _ptr(gathered_x), _ptr(gathered_scale), _ptr(recv_x),
+        _ptr(recv_scale), ctypes.byref(m), _stream(stream)))
 
 
 def moe_expert_standin(h: Handle, recv_x, recv_scale, expert_scale, y, stream=None) -> None:

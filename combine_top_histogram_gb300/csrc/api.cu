@@ -392,6 +392,51 @@ int moe_dispatch_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end, 
   return dispatch_range(h, token_begin, token_end, x, w, recv_x, recv_scale, meta, stream);
 }
 
+int moe_dispatch_allgather(moe_handle_t h, const void* x, const float* w, void* gathered_x,
+                           float* gathered_scale, void* recv_x, float* recv_scale,
+                           const moe_recv_meta_t* meta, void* stream) {
+  if (!h || !x || !w || !gathered_x || !recv_x || !meta) return MOE_ERR_INVALID_ARG;
+  if (!meta->local_expert || !meta->src_rank || !meta->src_token || !meta->slot || !meta->weight)
+    return MOE_ERR_INVALID_ARG;
+  const bool fp8 = h->cfg.dispatch_dtype == MOE_FP8_E4M3;
+  if (fp8 && (!recv_scale || !gathered_scale)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(gathered_x, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (h->layout_gen == 0) return MOE_ERR_STATE;
+  moe::AllGatherArgs g{};
+  moe::DispatchArgs& a = g.dis;
+  a.x = static_cast<const uint16_t*>(x);
+  a.w = w;
+  a.acode = h->acode;
+  a.hist = h->hist;
+  a.expert_offset = h->expert_offset;
+  a.inv = h->inv;
+  a.recv = recv_x;
+  a.recv_scale = recv_scale;
+  a.m_local_expert = meta->local_expert;
+  a.m_src_rank = meta->src_rank;
+  a.m_src_token = meta->src_token;
+  a.m_slot = meta->slot;
+  a.m_weight = meta->weight;
+  a.T = h->T;
+  a.Tr = h->cfg.tokens_per_rank;
+  a.k = h->cfg.top_k;
+  a.E = h->cfg.num_experts;
+  a.L = h->L;
+  a.H = h->cfg.hidden;
+  a.tpc = h->cur_tpc;
+  a.cps = h->cur_cps;
+  a.nchunks = h->cfg.num_ranks * h->cur_cps;
+  a.cap = h->cfg.expert_capacity;
+  g.gathered = gathered_x;
+  g.gathered_scale = gathered_scale;
+  g.P = h->cfg.num_ranks;
+  const int rc =
+      cuda_rc(moe::launch_allgather(g, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
+  if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
+  return rc;
+}
+
 int moe_set_wait_limit(moe_handle_t h, int64_t polls) {
   if (!h || polls < 0) return MOE_ERR_INVALID_ARG;
   h->wait_limit = polls;

@@ -34,7 +34,8 @@ constexpr int kDispatchThreads = 128;
 
 // Resolves the k receive rows of token g into rows_s, writes inv and the row
 // metadata. Threads 0..k-1 each take one slot.
-__device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g, int* rows_s) {
+__device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g, int* rows_s,
+                                             int* owner_s = nullptr) {
   const int j = threadIdx.x;
   if (j >= p.k) return;
   const long long a = g * p.k + j;
@@ -56,6 +57,7 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
     }
   }
   p.inv[a] = r;
+  if (owner_s) owner_s[j] = code >= 0 ? code_expert(code) / p.L : 0;
   int dst = r;
   if (p.send_pos && r >= 0) {
     const long long se = (long long)code_expert(code) + (long long)(g / p.Tr) * p.E;
@@ -161,7 +163,105 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const Dispatc
   }
 }
 
+// AllGather comparator, stage 1: every token row (quantised once for FP8) is
+// written to all P ranks' gathered copies, rows d*T + g.
+template <bool FP8, int VPT>
+__global__ void __launch_bounds__(kDispatchThreads) k_allgather(const AllGatherArgs a) {
+  const DispatchArgs& p = a.dis;
+  const int nvec = p.H >> 3, nblk = p.H >> 7, tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
+    for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
+      uint4 val[VPT];
+      float sc[VPT];
+      uint2 code[VPT];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int v = v0 + i * kDispatchThreads + tid;
+        val[i] = v < nvec ? ld_stream(src + v) : make_uint4(0u, 0u, 0u, 0u);
+        if (FP8) {
+          float m = amax8(val[i]);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          sc[i] = __fdiv_rn(m, 448.0f);
+          code[i] = quant8(val[i], sc[i], m == 0.0f);
+        }
+      }
+      for (int d = 0; d < a.P; ++d) {
+        const long long row = (long long)d * p.T + g;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = v0 + i * kDispatchThreads + tid;
+          if (v >= nvec) continue;
+          if (FP8) {
+            reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.gathered) + row * p.H)[v] = code[i];
+            if ((tid & 15) == 0) a.gathered_scale[row * nblk + (v >> 4)] = sc[i];
+          } else {
+            reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.gathered) + row * p.H)[v] = val[i];
+          }
+        }
+      }
+    }
+  }
+}
+
+// Stage 2, the local filter: every kept assignment copies its token's row from
+// the gathered copy of the rank that owns its expert, into the same receive
+// row (with the same metadata and inv) as the fused dispatch.
+template <bool FP8>
+__global__ void __launch_bounds__(kDispatchThreads) k_allgather_filter(const AllGatherArgs a) {
+  __shared__ int rows_s[MOE_MAX_TOPK];
+  __shared__ int owner_s[MOE_MAX_TOPK];
+  const DispatchArgs& p = a.dis;
+  const long long rb = FP8 ? (long long)p.H : 2ll * p.H;  // payload bytes per row
+  const int row_vec = (int)(rb >> 4);                     // 16-byte vectors per row
+  const int nblk = p.H >> 7;
+  pdl_wait();
+  pdl_trigger();
+  for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
+    resolve_rows(p, g, rows_s, owner_s);
+    __syncthreads();
+    for (int j = 0; j < p.k; ++j) {
+      const int r = rows_s[j];
+      if (r < 0) continue;
+      const long long srow = (long long)owner_s[j] * p.T + g;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.gathered) + srow * rb);
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.recv) + (long long)r * rb);
+      for (int v = threadIdx.x; v < row_vec; v += blockDim.x) dst[v] = __ldcs(src + v);
+      if (FP8)
+        for (int q = threadIdx.x; q < nblk; q += blockDim.x)
+          p.recv_scale[(long long)r * nblk + q] = __ldcs(a.gathered_scale + srow * nblk + q);
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_allgather(const AllGatherArgs& a, bool fp8, int num_sms, cudaStream_t st) {
+  if (a.dis.T <= 0) return cudaSuccess;
+  long long blocks = a.dis.T;
+  const long long cap = (long long)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  const dim3 grid((int)blocks), block(kDispatchThreads);
+  const int nvec = a.dis.H >> 3;
+  cudaError_t err;
+  if (fp8) {
+    err = nvec <= 128   ? launch_pdl(k_allgather<true, 1>, grid, block, 0, st, a)
+          : nvec <= 512 ? launch_pdl(k_allgather<true, 4>, grid, block, 0, st, a)
+                        : launch_pdl(k_allgather<true, 8>, grid, block, 0, st, a);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k_allgather_filter<true>, grid, block, 0, st, a);
+  }
+  err = nvec <= 128   ? launch_pdl(k_allgather<false, 1>, grid, block, 0, st, a)
+        : nvec <= 512 ? launch_pdl(k_allgather<false, 4>, grid, block, 0, st, a)
+                      : launch_pdl(k_allgather<false, 8>, grid, block, 0, st, a);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(k_allgather_filter<false>, grid, block, 0, st, a);
+}
 
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st) {
   if (a.T - a.g0 <= 0) return cudaSuccess;

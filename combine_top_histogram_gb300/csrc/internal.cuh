@@ -90,6 +90,15 @@ struct FusedArgs {
   int xs_offset_ints;     // where they start in dynamic shared memory
 };
 
+// AllGather-style comparator: every virtual rank holds a copy of all tokens
+// (gathered rows d*T + g), then keeps the assignments to its own experts.
+struct AllGatherArgs {
+  DispatchArgs dis;
+  void* gathered;         // [P*T] rows (bf16, or e4m3 codes)
+  float* gathered_scale;  // [P*T, H/128] (FP8)
+  int P;
+};
+
 struct A2avArgs {
   const void* send;          // send pool rows
   const float* send_scale;   // FP8 scale rows of the send pool, or null
@@ -169,6 +178,7 @@ cudaError_t launch_standin_tokens(const StandinArgs& a, int num_sms, cudaStream_
 cudaError_t launch_send_pos(const int32_t* kept_cnt, int32_t* send_pos, int32_t* src_base, int P,
                             int E, cudaStream_t st);
 cudaError_t launch_a2av(const A2avArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_allgather(const AllGatherArgs& a, bool fp8, int num_sms, cudaStream_t st);
 size_t fused_smem_bytes(int E, int tpc, int k, int H, int P, bool prefetch_x,
                         int* xs_offset_ints);
 cudaError_t fused_prepare(bool route, bool fp8, int E, size_t smem, int* blocks_per_sm);

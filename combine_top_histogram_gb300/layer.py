@@ -65,6 +65,19 @@ class MoeLayer:
         B.moe_dispatch_two_stage(self.handle, x, w, self.send_x, self.send_scale, self.recv_x,
                                  self.recv_scale, self.meta, stream)
 
+    def dispatch_allgather(self, x, w, stream=None):
+        """The AllGather comparator: all tokens to every rank, then a local filter."""
+        import torch
+        if getattr(self, "gathered_x", None) is None:
+            dt = torch.uint8 if self.fp8 else torch.bfloat16
+            self.gathered_x = torch.empty((self.P * self.T, self.H), dtype=dt,
+                                          device=self.out.device)
+            self.gathered_scale = (torch.empty((self.P * self.T, self.H // 128),
+                                               dtype=torch.float32, device=self.out.device)
+                                   if self.fp8 else None)
+        B.moe_dispatch_allgather(self.handle, x, w, self.gathered_x, self.gathered_scale,
+                                 self.recv_x, self.recv_scale, self.meta, stream)
+
     def layout_dispatch_fused(self, x, ids=None, w=None, logits=None, stream=None):
         """One persistent launch: route (logits) or take ids/w, lay out, dispatch."""
         if logits is not None:
@@ -80,7 +93,7 @@ class MoeLayer:
         B.moe_combine(self.handle, self.y, w, self.out, stream)
 
     def forward(self, x, ids=None, w=None, logits=None, expert_scale=None, stream=None,
-                two_stage=False, fused=False):
+                two_stage=False, fused=False, allgather=False):
         """Whole layer; with logits the routed ids/weights land in self.ids / self.w.
         two_stage=True dispatches through the two-stage comparator."""
         if fused:
@@ -95,7 +108,9 @@ class MoeLayer:
             w = self.w
         else:
             self.layout(ids, stream)
-        if two_stage:
+        if allgather:
+            self.dispatch_allgather(x, w, stream)
+        elif two_stage:
             self.dispatch_two_stage(x, w, stream)
         else:
             self.dispatch(x, w, stream)

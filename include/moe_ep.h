@@ -199,6 +199,17 @@ int moe_get_layout(moe_handle_t h, moe_layout_view_t *out);
 int moe_dispatch(moe_handle_t h, const void *x, const float *w, void *recv_x,
                  float *recv_scale, const moe_recv_meta_t *meta, void *stream);
 
+/* NEXT-row comparator, the AllGather-style dispatcher ([EP] "Why not collect
+ * all tokens with AllGather"): every rank first receives every token
+ * (gathered_x: P*T rows, rank d's copy of token g at row d*T + g; FP8 rows are
+ * quantised once and copied with their scales into gathered_scale
+ * [P*T, H/128], NULL for BF16), then keeps the assignments to its own
+ * experts. Same receive rows, metadata and inv as moe_dispatch; T*P rows
+ * cross the "network" instead of T*k. */
+int moe_dispatch_allgather(moe_handle_t h, const void *x, const float *w, void *gathered_x,
+                           float *gathered_scale, void *recv_x, float *recv_scale,
+                           const moe_recv_meta_t *meta, void *stream);
+
 /* Persistent single-launch path for small, latency-bound layers (decode):
  * route (logits != NULL: ids and w are written, as moe_route_dispatch_layout)
  * or take given ids and w (logits == NULL), build the layout and dispatch the

@@ -25,7 +25,7 @@ def to_np_bits(t):
 
 def run_gpu(wl: W.Workload, inp: W.Inputs, ids=None, layer=None, stream=None,
             copy_rows: bool = True, two_stage: bool = False, fused: bool = False,
-            pipelined: int = 0):
+            pipelined: int = 0, allgather: bool = False):
     """The path on the GPU through the C ABI; returns host copies of everything
     (copy_rows=False leaves the row buffers on the device, in res["layer"])."""
     import torch
@@ -48,14 +48,14 @@ def run_gpu(wl: W.Workload, inp: W.Inputs, ids=None, layer=None, stream=None,
     elif ids is None and inp.logits is not None:
         logits = torch.from_numpy(inp.logits).to(dev)
         layer.forward(x, logits=logits, expert_scale=c, stream=stream, two_stage=two_stage,
-                      fused=fused)
+                      fused=fused, allgather=allgather)
         w_used = layer.w
     else:
         ids_np = inp.ids if ids is None else ids
         ids_t = torch.from_numpy(np.ascontiguousarray(ids_np, np.int32)).to(dev)
         w_used = torch.from_numpy(inp.w).to(dev)
         layer.forward(x, ids=ids_t, w=w_used, expert_scale=c, stream=stream, two_stage=two_stage,
-                      fused=fused)
+                      fused=fused, allgather=allgather)
     torch.cuda.synchronize()
     view = layer.layout_view()
     res = {k: to_np_bits(v) for k, v in view.items()}
