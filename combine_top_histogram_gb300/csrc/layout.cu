@@ -13,8 +13,9 @@
 // Design (one GPU, P virtual ranks in one HBM):
 //   * The assignment list (s, t, j) is cut into chunks of whole tokens that
 //     never straddle a source rank. One CTA per chunk.
-//   * Route mode: a warp routes 32/k tokens (k rounded up to a power of
-//     two): for each it holds the E logits as order-preserving keys in
+//   * Route mode: a warp routes one token when chunks are small (latency) and
+//     up to 32/k tokens (k rounded up to a power of two) when there are many
+//     (fewer instructions per token): for each it holds the E logits as order-preserving keys in
 //     registers (E/32 per lane) and picks the top-k by k rounds of a warp
 //     max-reduction plus a min-reduction over tied expert indices (value
 //     descending, expert ascending on ties); then all their softmax weights
@@ -26,10 +27,14 @@
 //     re-walks the sub-range and gives each assignment its stable rank = warp
 //     base + lanes of the same expert below it. No atomics decide any
 //     position, so the layout is deterministic.
-//   * The chunk histogram goes to global memory; the last CTA to arrive
-//     (threadfence + arrival counter, no spinning) scans all chunk histograms
-//     and derives n_e, expert_offset, cnt[s][e], C[s][d], send_offset,
-//     recv_offset and rank_base, applying the capacity clamp.
+//   * The chunk histogram goes to global memory transposed, [E][nchunks]. A
+//     second kernel (k_scan) scans it with one warp per expert column, and its
+//     last CTA to arrive (threadfence + arrival counter, no spinning) derives
+//     n_e, expert_offset, cnt[s][e], C[s][d], send_offset, recv_offset and
+//     rank_base, applying the capacity clamp. Both kernels use programmatic
+//     dependent launch, so the scan's CTAs are resident before the counts land.
+//   * The device pieces shared with the persistent path live in
+//     layout_device.cuh.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
