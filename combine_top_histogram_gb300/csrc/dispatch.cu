@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const Dispatc
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         sc[i] = __fdiv_rn(m, 448.0f);
-        code[i] = quant8(val[i], sc[i], m == 0.0f);
+        code[i] = quant8(val[i], sc[i], m);
       }
       for (int j = 0; j < p.k; ++j) {
         const int r = rows_s[j];
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kDispatchThreads) k_allgather(const AllGatherA
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
           sc[i] = __fdiv_rn(m, 448.0f);
-          code[i] = quant8(val[i], sc[i], m == 0.0f);
+          code[i] = quant8(val[i], sc[i], m);
         }
       }
       for (int d = 0; d < a.P; ++d) {

@@ -179,7 +179,7 @@ __device__ __forceinline__ bool fused_body(const FusedArgs& f, int* smem) {
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         const float sc = __fdiv_rn(m, 448.0f);
-        const uint2 code = quant8(val, sc, m == 0.0f);
+        const uint2 code = quant8(val, sc, m);
         if (on) {
           for (int j = 0; j < p.k; ++j) {
             const int r = rows_s[tl * p.k + j];
