@@ -33,7 +33,7 @@ EXPORTED_SYMBOLS = (
     "moe_dispatch_layout_noalloc", "moe_copy_h2d_async", "moe_copy_d2h_async",
     "moe_dispatch_two_stage", "moe_layout_dispatch_fused", "moe_set_wait_limit",
     "moe_dispatch_tokens", "moe_expert_standin_tokens", "moe_combine_tokens",
-    "moe_dispatch_allgather",
+    "moe_dispatch_allgather", "moe_layout_tables",
 )
 
 
@@ -97,6 +97,8 @@ def load_library():
         lib.moe_dispatch_layout.argtypes = [vp, vp, vp]
         lib.moe_route_dispatch_layout.restype = i32
         lib.moe_route_dispatch_layout.argtypes = [vp, vp, vp, vp, vp]
+        lib.moe_layout_tables.restype = i32
+        lib.moe_layout_tables.argtypes = [vp, vp]
         lib.moe_get_layout.restype = i32
         lib.moe_get_layout.argtypes = [vp, ctypes.POINTER(moe_layout_view_t)]
         lib.moe_dispatch.restype = i32
@@ -227,6 +229,11 @@ def moe_dispatch_layout(h: Handle, ids, stream=None) -> None:
 def moe_route_dispatch_layout(h: Handle, logits, ids, w, stream=None) -> None:
     _check("moe_route_dispatch_layout", load_library().moe_route_dispatch_layout(
         h.ptr, _ptr(logits), _ptr(ids), _ptr(w), _stream(stream)))
+
+
+def moe_layout_tables(h: Handle, stream=None) -> None:
+    """Completes the per-source tables of the last layout without dispatching."""
+    _check("moe_layout_tables", load_library().moe_layout_tables(h.ptr, _stream(stream)))
 
 
 def moe_get_layout(h: Handle) -> dict:

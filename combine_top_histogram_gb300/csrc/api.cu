@@ -139,7 +139,32 @@ moe::LayoutArgs layout_args(moe_handle_t h, bool route) {
   a.nchunks = a.P * a.cps;
   a.cap = h->cfg.expert_capacity;
   a.Na = h->Na;
+  a.defer_tables = 1;
   return a;
+}
+
+moe::TablesArgs tables_args(moe_handle_t h) {
+  moe::TablesArgs t{};
+  t.src_pre = h->src_pre;
+  t.expert_offset = h->expert_offset;
+  t.cnt = h->cnt;
+  t.kept_cnt = h->kept_cnt;
+  t.recv_offset = h->recv_offset;
+  t.C = h->C;
+  t.send_offset = h->send_offset;
+  t.P = h->cfg.num_ranks;
+  t.E = h->cfg.num_experts;
+  t.L = h->L;
+  t.cap = h->cfg.expert_capacity;
+  return t;
+}
+
+// Builds the per-source tables of the last layout if no launch has yet.
+int ensure_tables(moe_handle_t h, cudaStream_t st) {
+  if (!h->tables_pending) return MOE_OK;
+  const int rc = cuda_rc(moe::launch_tables(tables_args(h), st));
+  if (rc == MOE_OK) h->tables_pending = 0;
+  return rc;
 }
 
 }  // namespace
@@ -246,6 +271,7 @@ static int run_layout(moe_handle_t h, bool route, const int32_t* ids_in, const f
   h->cur_tpc = a.tpc;
   h->cur_cps = a.cps;
   h->layout_gen += 1;
+  h->tables_pending = 1;
   return MOE_OK;
 }
 
@@ -258,6 +284,12 @@ int moe_route_dispatch_layout(moe_handle_t h, const float* logits, int32_t* ids,
                               void* stream) {
   if (!h || !logits || !ids || !w) return MOE_ERR_INVALID_ARG;
   return run_layout(h, true, nullptr, logits, ids, w, stream);
+}
+
+int moe_layout_tables(moe_handle_t h, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (h->layout_gen == 0) return MOE_ERR_STATE;
+  return ensure_tables(h, static_cast<cudaStream_t>(stream));
 }
 
 int moe_get_layout(moe_handle_t h, moe_layout_view_t* out) {
@@ -311,8 +343,15 @@ static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void
   a.cps = h->cur_cps;
   a.nchunks = h->cfg.num_ranks * h->cur_cps;
   a.cap = h->cfg.expert_capacity;
+  if (h->tables_pending) {  // built by the launch's first P CTAs
+    a.tab = tables_args(h);
+    a.tab_ctas = h->cfg.num_ranks;
+  }
   const int rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
-  if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
+  if (rc == MOE_OK) {
+    h->dispatch_gen = h->layout_gen;
+    h->tables_pending = 0;
+  }
   return rc;
 }
 
@@ -327,8 +366,10 @@ int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* 
   if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(send_x, 16)) return MOE_ERR_INVALID_ARG;
   if (h->layout_gen == 0) return MOE_ERR_STATE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc = cuda_rc(moe::launch_send_pos(h->kept_cnt, h->send_pos, h->src_base,
-                                        h->cfg.num_ranks, h->cfg.num_experts, st));
+  int rc = ensure_tables(h, st);  // the send positions come from kept_cnt
+  if (rc != MOE_OK) return rc;
+  rc = cuda_rc(moe::launch_send_pos(h->kept_cnt, h->send_pos, h->src_base,
+                                    h->cfg.num_ranks, h->cfg.num_experts, st));
   if (rc != MOE_OK) return rc;
   moe::DispatchArgs a{};
   a.x = static_cast<const uint16_t*>(x);
@@ -431,8 +472,9 @@ int moe_dispatch_allgather(moe_handle_t h, const void* x, const float* w, void* 
   g.gathered = gathered_x;
   g.gathered_scale = gathered_scale;
   g.P = h->cfg.num_ranks;
-  const int rc =
-      cuda_rc(moe::launch_allgather(g, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
+  int rc = ensure_tables(h, static_cast<cudaStream_t>(stream));
+  if (rc != MOE_OK) return rc;
+  rc = cuda_rc(moe::launch_allgather(g, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
   if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
   return rc;
 }
@@ -473,6 +515,7 @@ int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids,
   if (per_sm < 1) return MOE_ERR_UNSUPPORTED;
   moe::FusedArgs f{};
   f.lay = layout_args(h, route);
+  f.lay.defer_tables = 0;  // the persistent kernel builds every table itself
   f.lay.ids_in = ids;
   f.lay.logits = logits;
   f.lay.ids_out = ids;
@@ -514,6 +557,7 @@ int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids,
   h->cur_cps = cps;
   h->layout_gen += 1;
   h->dispatch_gen = h->layout_gen;
+  h->tables_pending = 0;
   return MOE_OK;
 }
 

@@ -20,17 +20,39 @@
 //     r = expert_offset[e] + chunk_base[chunk][e] + chunk-local rank
 // (the stable (expert, source, token, slot) order) and is kept iff its
 // in-expert position is below the capacity.
+//
+// Nothing in the copy needs the per-source tables (cnt, kept counts, receive
+// offsets per source, C and the send offsets), so when the layout deferred
+// them the first P CTAs of the launch build them, one source rank each, while
+// the other CTAs copy tokens; they are complete when the dispatch is.
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "internal.cuh"
 #include "payload_device.cuh"
+#include "tables_device.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kDispatchThreads = 128;
+
+// CTA blockIdx.x < p.tab_ctas of a dispatch launch: the tables of source
+// rank blockIdx.x (dynamic shared memory: E + 32 ints).
+__device__ void tables_cta(const DispatchArgs& p) {
+  extern __shared__ int tab_s[];
+  pdl_wait();
+  pdl_trigger();
+  source_tables(p.tab, blockIdx.x, tab_s);
+}
+
+__global__ void __launch_bounds__(kDispatchThreads) k_tables(const TablesArgs t) {
+  extern __shared__ int tab_s[];
+  pdl_wait();
+  pdl_trigger();
+  source_tables(t, blockIdx.x, tab_s);
+}
 
 // Resolves the k receive rows of token g into rows_s, writes inv and the row
 // metadata. Threads 0..k-1 each take one slot.
@@ -67,12 +89,17 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
 }
 
 template <int VPT>
-__global__ void __launch_bounds__(kDispatchThreads) k_dispatch_bf16(const DispatchArgs p) {
+__global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const DispatchArgs p) {
   __shared__ int rows_s[MOE_MAX_TOPK];
   const int nvec = p.H >> 3;  // 16-byte vectors per row
   const int tid = threadIdx.x;
   bool waited = false;
-  for (long long g = p.g0 + blockIdx.x; g < p.T; g += gridDim.x) {
+  if ((int)blockIdx.x < p.tab_ctas) {
+    tables_cta(p);
+    return;
+  }
+  const long long nb = gridDim.x - p.tab_ctas;
+  for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -110,13 +137,18 @@ __global__ void __launch_bounds__(kDispatchThreads) k_dispatch_bf16(const Dispat
 // lanes (blockDim and the vector stride are multiples of 16), so the block's
 // amax is a 4-step xor-shuffle reduction inside each half-warp.
 template <int VPT>
-__global__ void __launch_bounds__(kDispatchThreads) k_dispatch_fp8(const DispatchArgs p) {
+__global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const DispatchArgs p) {
   __shared__ int rows_s[MOE_MAX_TOPK];
   const int nvec = p.H >> 3;
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
   bool waited = false;
-  for (long long g = p.g0 + blockIdx.x; g < p.T; g += gridDim.x) {
+  if ((int)blockIdx.x < p.tab_ctas) {
+    tables_cta(p);
+    return;
+  }
+  const long long nb = gridDim.x - p.tab_ctas;
+  for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -264,21 +296,29 @@ cudaError_t launch_allgather(const AllGatherArgs& a, bool fp8, int num_sms, cuda
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st) {
-  if (a.T - a.g0 <= 0) return cudaSuccess;
-  long long blocks = a.T - a.g0;
+  long long blocks = a.T - a.g0 < 0 ? 0 : a.T - a.g0;
   const long long cap = (long long)num_sms * 16;  // 16 CTAs of 128 threads fill an SM
   if (blocks > cap) blocks = cap;
+  if (blocks == 0 && a.tab_ctas == 0) return cudaSuccess;
+  if (blocks == 0) return launch_tables(a.tab, st);
+  const dim3 grid((int)(blocks + a.tab_ctas)), block(kDispatchThreads);
+  const size_t smem = a.tab_ctas > 0 ? (size_t)(a.tab.E + 32) * sizeof(int) : 0;
   const int nvec = a.H >> 3;
   if (fp8) {
-    if (nvec <= 128) return launch_pdl(k_dispatch_fp8<1>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
-    else if (nvec <= 512) return launch_pdl(k_dispatch_fp8<4>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
-    else return launch_pdl(k_dispatch_fp8<8>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
+    if (nvec <= 128) return launch_pdl(k_dispatch_fp8<1>, grid, block, smem, st, a);
+    else if (nvec <= 512) return launch_pdl(k_dispatch_fp8<4>, grid, block, smem, st, a);
+    else return launch_pdl(k_dispatch_fp8<8>, grid, block, smem, st, a);
   } else {
-    if (nvec <= 128) return launch_pdl(k_dispatch_bf16<1>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
-    else if (nvec <= 512) return launch_pdl(k_dispatch_bf16<4>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
-    else return launch_pdl(k_dispatch_bf16<8>, dim3((int)blocks), dim3(kDispatchThreads), 0, st, a);
+    if (nvec <= 128) return launch_pdl(k_dispatch_bf16<1>, grid, block, smem, st, a);
+    else if (nvec <= 512) return launch_pdl(k_dispatch_bf16<4>, grid, block, smem, st, a);
+    else return launch_pdl(k_dispatch_bf16<8>, grid, block, smem, st, a);
   }
-  return cudaGetLastError();
+}
+
+cudaError_t launch_tables(const TablesArgs& t, cudaStream_t st) {
+  if (t.P <= 0) return cudaSuccess;
+  return launch_pdl(k_tables, dim3(t.P), dim3(kDispatchThreads), (size_t)(t.E + 32) * sizeof(int),
+                    st, t);
 }
 
 }  // namespace moe

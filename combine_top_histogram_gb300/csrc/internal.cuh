@@ -53,6 +53,23 @@ struct LayoutArgs {
   int tpc, cps, nchunks;  // tokens per chunk, chunks per source rank, chunks
   int cap;                // 0 = unlimited
   long long Na;
+  // 1: the scan's last CTA writes only n_kept/n_raw-derived outputs (expert
+  // offsets, rank bases, totals); the per-source tables are left to
+  // source_tables (dispatch CTAs or k_tables). 0: it writes every table.
+  int defer_tables;
+};
+
+// Per-source tables of the layout, one source rank s per CTA (source_tables):
+// cnt[s][e], kept_cnt[s][e], recv_offset[s][e], C[s][d], send_offset[s][d].
+struct TablesArgs {
+  const int32_t* src_pre;        // [(P+1)*E]
+  const int32_t* expert_offset;  // [E+1]
+  int32_t* cnt;
+  int32_t* kept_cnt;
+  int32_t* recv_offset;
+  int32_t* C;
+  int32_t* send_offset;
+  int P, E, L, cap;
 };
 
 struct DispatchArgs {
@@ -78,6 +95,10 @@ struct DispatchArgs {
   const int32_t* send_pos;
   const int32_t* src_base;
   const int32_t* recv_offset;
+  // tab_ctas > 0: the first tab_ctas CTAs build the per-source tables (one
+  // source each) while the others copy tokens.
+  TablesArgs tab;
+  int tab_ctas;
 };
 
 // Persistent single-launch route/layout/dispatch (fused.cu).
@@ -172,6 +193,7 @@ size_t layout_smem_bytes(int E, int tpc, int k, int P);
 size_t scan_smem_bytes(int E, int P);
 cudaError_t layout_prepare(int E, int tpc, int k, int P);
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st);
+cudaError_t launch_tables(const TablesArgs& t, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_standin(const StandinArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_standin_tokens(const StandinArgs& a, int num_sms, cudaStream_t st);
@@ -204,5 +226,6 @@ struct moe_handle {
   int32_t *n_raw, *n_kept, *expert_offset, *cnt, *kept_cnt, *C, *send_offset,
       *recv_offset, *rank_base, *hist, *src_pre, *acode, *inv, *send_pos, *src_base;
   unsigned long long layout_gen, dispatch_gen;
+  int tables_pending;       // per-source tables of the last layout not yet built
   long long wait_limit;     // bounded device waits (persistent path)
 };

@@ -10,11 +10,10 @@
 
 #include "ffmath.cuh"
 #include "internal.cuh"
+#include "tables_device.cuh"
 
 namespace moe {
 namespace {
-
-constexpr unsigned kFull = 0xffffffffu;
 
 // Lanes of the warp holding the same expert id as this lane (valid ids >= 0),
 // from one ballot per bit of the id: the bit-plane form of a warp multisplit
@@ -27,45 +26,6 @@ __device__ __forceinline__ unsigned peer_mask(int e, int nbits) {
     m &= bit ? bb : ~bb;
   }
   return m;
-}
-
-// Exclusive scan in place of a[0..n) held in shared memory, by the whole CTA.
-// tmp: 32 ints of shared scratch. Returns the total. Ends with __syncthreads.
-__device__ int cta_exclusive_scan(int* a, int n, int* tmp) {
-  const int nt = blockDim.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per = (n + nt - 1) / nt;
-  const int b0 = min(n, (int)threadIdx.x * per), b1 = min(n, b0 + per);
-  int local = 0;
-  for (int i = b0; i < b1; ++i) local += a[i];
-  int v = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int u = __shfl_up_sync(kFull, v, o);
-    if (lane >= o) v += u;
-  }
-  if (lane == 31) tmp[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = nt >> 5;
-    int x = lane < nw ? tmp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int u = __shfl_up_sync(kFull, x, o);
-      if (lane >= o) x += u;
-    }
-    tmp[lane] = x;
-  }
-  __syncthreads();
-  int run = v - local + (warp > 0 ? tmp[warp - 1] : 0);
-  const int total = tmp[(nt >> 5) - 1];
-  for (int i = b0; i < b1; ++i) {
-    int t = a[i];
-    a[i] = run;
-    run += t;
-  }
-  __syncthreads();
-  return total;
 }
 
 // Order-preserving map of a finite float to an unsigned key (larger float ->
@@ -186,7 +146,9 @@ __device__ __forceinline__ void route_group_warp(const float* __restrict__ logit
 // The layout tables, by the last CTA of the scan kernel: reads n_kept,
 // n_raw and the per-(source, expert) prefixes into shared memory, scans the
 // kept counts in global expert order (expert offsets) and derives every
-// per-(source, expert) and per-(source, rank) table and the totals.
+// per-(source, expert) and per-(source, rank) table and the totals. With
+// p.defer_tables it writes only the expert offsets, rank bases and totals
+// (what the dispatch needs), and source_tables builds the rest later.
 __device__ void layout_tables(const LayoutArgs& p, int* smem) {
   const int E = p.E, P = p.P, tid = threadIdx.x, NT = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5;
@@ -201,7 +163,8 @@ __device__ void layout_tables(const LayoutArgs& p, int* smem) {
     sk[e] = __ldcg(p.n_kept + e);
     sraw[e] = __ldcg(p.n_raw + e);
   }
-  for (int i = tid; i < (P + 1) * E; i += NT) pre[i] = __ldcg(p.src_pre + i);
+  if (!p.defer_tables)
+    for (int i = tid; i < (P + 1) * E; i += NT) pre[i] = __ldcg(p.src_pre + i);
   __syncthreads();
   {
     int dr = 0, rw = 0;
@@ -216,6 +179,14 @@ __device__ void layout_tables(const LayoutArgs& p, int* smem) {
   const int total = cta_exclusive_scan(sk, E, tmp);
   for (int e = tid; e <= E; e += NT) p.expert_offset[e] = e < E ? sk[e] : total;
   for (int d = tid; d <= P; d += NT) p.rank_base[d] = d < P ? sk[d * p.L] : total;
+  if (tid == 0) {
+    p.totals[0] = total;
+    p.totals[1] = red[0];
+    p.totals[2] = (int)(p.Na - (long long)red[1]);
+    p.totals[3] = 0;
+    *p.done = 0u;  // ready for the next layout on this workspace
+  }
+  if (p.defer_tables) return;
   auto kept_of = [&](int s, int e) {
     const int a = pre[s * E + e];
     const int c = pre[(s + 1) * E + e] - a;
@@ -267,13 +238,6 @@ __device__ void layout_tables(const LayoutArgs& p, int* smem) {
       if (d < P) p.send_offset[(long long)s * P + d] = carry + x - v;
       carry += __shfl_sync(kFull, x, 31);
     }
-  }
-  if (tid == 0) {
-    p.totals[0] = total;
-    p.totals[1] = red[0];
-    p.totals[2] = (int)(p.Na - (long long)red[1]);
-    p.totals[3] = 0;
-    *p.done = 0u;  // ready for the next layout on this workspace
   }
 }
 

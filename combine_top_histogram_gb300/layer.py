@@ -51,6 +51,11 @@ class MoeLayer:
     def layout(self, ids, stream=None):
         B.moe_dispatch_layout(self.handle, ids, stream)
 
+    def layout_tables(self, stream=None):
+        """Per-source tables of the last layout without dispatching (a dispatch
+        builds them in its own launch)."""
+        B.moe_layout_tables(self.handle, stream)
+
     def dispatch(self, x, w, stream=None):
         B.moe_dispatch(self.handle, x, w, self.recv_x, self.recv_scale, self.meta, stream)
 

@@ -100,8 +100,19 @@ typedef struct {
 /* Opaque handle: configuration + pointers into the caller's workspace. */
 typedef struct moe_handle *moe_handle_t;
 
-/* Device pointers to the layout inside the workspace, valid after
- * moe_dispatch_layout (counts/offsets) and moe_dispatch (inv). All int32.
+/* Device pointers to the layout inside the workspace. All int32. When each
+ * array is complete, in stream order:
+ *   - expert_count, expert_count_raw, expert_offset, rank_base, totals: after
+ *     the layout call (moe_dispatch_layout, moe_route_dispatch_layout);
+ *   - src_expert_count, src_expert_kept, count_matrix, send_offset,
+ *     recv_offset (the per-source tables): after the dispatch that follows the
+ *     layout. The copy does not need them, so moe_dispatch and
+ *     moe_dispatch_tokens build them in the same launch, beside the copy;
+ *     moe_dispatch_two_stage and moe_dispatch_allgather build them first. A
+ *     caller that wants them without dispatching calls moe_layout_tables;
+ *   - inv: after the dispatch;
+ *   - everything: after moe_layout_dispatch_fused and
+ *     moe_dispatch_layout_noalloc.
  *   expert_count[E]       n_e: receive rows of expert e after capacity
  *   expert_count_raw[E]   valid assignments to e before capacity
  *   expert_offset[E+1]    first receive row of expert e; [E] = total rows.
@@ -184,6 +195,15 @@ int moe_dispatch_layout(moe_handle_t h, const int32_t *ids, void *stream);
  * ids and w) and builds the layout from the routed ids. */
 int moe_route_dispatch_layout(moe_handle_t h, const float *logits, int32_t *ids,
                               float *w, void *stream);
+
+/* Completes the per-source tables of the last layout on the handle
+ * (src_expert_count, src_expert_kept, count_matrix, send_offset, recv_offset;
+ * see moe_layout_view_t) without dispatching: one launch of P CTAs if no
+ * dispatch has built them yet, nothing otherwise. Their definitions are those
+ * of [EP] "All-to-All-v" (C[s][d]) and "Why count and permute before
+ * dispatch" (send_offset = exclusive prefix of send_count).
+ * Errors: INVALID_ARG, STATE (no layout yet), CUDA. */
+int moe_layout_tables(moe_handle_t h, void *stream);
 
 /* Layout pointers (device) of the handle's workspace. Host-only, no launch. */
 int moe_get_layout(moe_handle_t h, moe_layout_view_t *out);

@@ -58,6 +58,7 @@ def test_null_handles_are_rejected(cuda_lib):
     assert cuda_lib.moe_dispatch_layout(None, None, None) == -1
     assert cuda_lib.moe_combine(None, None, None, None, None) == -1
     assert cuda_lib.moe_route_topk(None, None, None, None, None) == -1
+    assert cuda_lib.moe_layout_tables(None, None) == -1
 
 
 def test_build_targets_sm103a_without_fast_math():

@@ -191,6 +191,47 @@ def test_layout_route_only_entry_point(gpu):
     assert f32_ulp_diff(w.cpu().numpy(), ow).max() <= 1
 
 
+def test_layout_tables_without_dispatch(gpu):
+    """The per-source tables (cnt, kept counts, C, send and receive offsets)
+    are left to the dispatch launch; moe_layout_tables builds them alone. With
+    a capacity, 32 sources and 256 experts, every table equals the oracle's; a
+    second call and a later dispatch (which then builds nothing) keep them."""
+    import torch
+    import oracle
+    from combine_top_histogram_gb300 import MoeLayer
+    from combine_top_histogram_gb300 import binding as B
+    from harness import LAYOUT_KEYS
+    wl = W.PREFILL.scaled("tables", Tr=50, H=128, cap=40)
+    inp = W.make_inputs(wl)
+    layer = MoeLayer(wl.P, wl.Tr, wl.E, wl.k, wl.H, wl.dispatch_dtype, wl.cap)
+    with pytest.raises(B.MoeError) as ei:
+        layer.layout_tables()  # no layout yet
+    assert ei.value.code == -5
+    layer.route_layout(torch.from_numpy(inp.logits).cuda())
+    layer.layout_tables()
+    layer.layout_tables()
+    torch.cuda.synchronize()
+    ids = layer.ids.cpu().numpy()
+    lay = oracle.layout(wl.P, wl.Tr, wl.E, wl.k, ids, wl.cap)
+    view = {k: v.cpu().numpy() for k, v in layer.layout_view().items()}
+    checked = 0
+    for gk, ok in LAYOUT_KEYS:
+        if gk == "inv":
+            continue
+        assert np.array_equal(view[gk].reshape(-1), lay[ok].reshape(-1)), gk
+        checked += 1
+    assert checked >= 9
+    assert view["totals"][:3].tolist() == lay["totals"].tolist()
+    x = torch.from_numpy(inp.x.view(np.int16)).cuda().view(torch.bfloat16)
+    layer.dispatch(x, layer.w)
+    torch.cuda.synchronize()
+    after = {k: v.cpu().numpy() for k, v in layer.layout_view().items()}
+    assert np.array_equal(after["inv"].reshape(-1), lay["inv"].reshape(-1))
+    for gk, _ in LAYOUT_KEYS:
+        if gk != "inv":
+            assert np.array_equal(after[gk], view[gk]), gk
+
+
 def test_repeated_calls_on_one_handle(gpu):
     """The arrival counter resets itself: a second layer on the same handle
     (different routing) is as exact as the first."""
