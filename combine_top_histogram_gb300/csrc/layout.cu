@@ -47,33 +47,55 @@ namespace moe {
 namespace {
 
 // Column scan of the chunk histograms, one warp per expert: the table is
-// [E][nchunks], so a warp reads its expert's column contiguously, turns it
-// into exclusive chunk bases in place (warp shuffle scan, carried across
-// 32-chunk steps), and records the prefix at each source rank's first chunk
-// and the expert's totals. The last CTA to arrive builds the tables.
+// [E][nchunks], so a warp reads its expert's column contiguously and turns it
+// into exclusive chunk bases in place. Each lane takes a contiguous run of up
+// to kScanRun chunks, issuing all its loads at once, so a column costs one
+// L2 round trip and one warp shuffle scan of the lanes' sums; longer columns
+// take further passes. The scan also records the prefix at each source
+// rank's first chunk and the expert's totals. The last CTA to arrive builds
+// the tables.
+constexpr int kScanRun = 8;
+
 __global__ void __launch_bounds__(kScanThreads) k_scan(const LayoutArgs p) {
   extern __shared__ int smem[];
   __shared__ int s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x * (kScanThreads / 32) + warp;
   pdl_wait();
-  pdl_trigger();
   if (e < p.E) {
     int* col = p.hist + (long long)e * p.nchunks;
+    const int n = p.nchunks;
+    const int m = min(kScanRun, (n + 31) / 32);  // chunks per lane and pass
     int carry = 0;
-    for (int c0 = 0; c0 < p.nchunks; c0 += 32) {
-      const int b = c0 + lane;
-      const int v = b < p.nchunks ? __ldcg(col + b) : 0;
-      int x = v;
+    for (int c0 = 0; c0 < n; c0 += 32 * m) {
+      const int b0 = c0 + lane * m;
+      int v[kScanRun];
+      int sum = 0;
+#pragma unroll
+      for (int i = 0; i < kScanRun; ++i) {
+        v[i] = (i < m && b0 + i < n) ? __ldcg(col + b0 + i) : 0;
+        sum += v[i];
+      }
+      int x = sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(kFull, x, o);
         if (lane >= o) x += y;
       }
-      const int excl = carry + x - v;
-      if (b < p.nchunks) {
-        col[b] = excl;
-        if (b % p.cps == 0) p.src_pre[(b / p.cps) * p.E + e] = excl;
+      int run = carry + x - sum;
+      // source rank and offset of chunk b0 (cps chunks per source)
+      int s = b0 / p.cps, r = b0 - s * p.cps;
+#pragma unroll
+      for (int i = 0; i < kScanRun; ++i) {
+        if (i < m && b0 + i < n) {
+          col[b0 + i] = run;
+          if (r == 0) p.src_pre[s * p.E + e] = run;
+        }
+        run += v[i];
+        if (++r == p.cps) {
+          r = 0;
+          ++s;
+        }
       }
       carry += __shfl_sync(kFull, x, 31);
     }
@@ -87,6 +109,10 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(const LayoutArgs p) {
   __syncthreads();
   if (threadIdx.x == 0) s_last = (atomicAdd(p.done, 1u) == gridDim.x - 1);
   __syncthreads();
+  // The dependent dispatch launches only now: its row loads, issued before
+  // its own wait, would otherwise compete with the column scans and the
+  // arrival atomics on the critical path.
+  pdl_trigger();
   if (!s_last) return;
   __threadfence();
   layout_tables(p, smem);
