@@ -13,8 +13,12 @@
 // and fast sum (Dekker 1971), error-free product via FMA; double-length
 // multiply / divide after Dekker 1971; exp by the Cody-Waite additive range
 // reduction d = n*ln2 + r with ln2 split into two floats, then the Taylor
-// series of exp(r) for |r| <= ln2/2 evaluated by Horner's rule. All constants
-// below are values of ln 2 and 1/i!, split into hi + lo parts at compile time.
+// series of exp(r) for |r| <= ln2/2: its terms of degree 0..7 in float-float
+// by Estrin's scheme (pairs c_i + c_{i+1} r, combined with r^2 and r^4, so the
+// dependency chain is three multiply-adds deep instead of thirteen), and the
+// terms of degree 8..13, below 2^-27, in plain fp32 by Horner's rule on r.hi,
+// added as r^8 * tail. All constants below are values of ln 2 and 1/i!, split
+// into hi + lo parts at compile time.
 #pragma once
 
 #include <math.h>
@@ -61,19 +65,15 @@ __device__ __forceinline__ F2 mul(F2 a, F2 b) {
   return fast_two_sum(p.hi, p.lo);
 }
 
-// a / b: quotient estimate, exact remainder of the double-length operands,
-// one correction step.
+// a / b: the fp32 quotient q1 (relative error <= 2^-24), the remainder
+// a - q1*b of the double-length operands, and one correction q2 = rem / b:
+// the error of q1 + q2 is of the order of 2^-47 relative.
 __device__ __forceinline__ F2 div(F2 a, F2 b) {
   const float q1 = __fdiv_rn(a.hi, b.hi);
   const F2 qb = mul(b, F2{q1, 0.0f});
-  F2 r = add(a, F2{-qb.hi, -qb.lo});
+  const F2 r = add(a, F2{-qb.hi, -qb.lo});
   const float q2 = __fdiv_rn(r.hi, b.hi);
-  F2 q = fast_two_sum(q1, q2);
-  // second correction for the last bits
-  const F2 qb2 = mul(b, q);
-  r = add(a, F2{-qb2.hi, -qb2.lo});
-  const float q3 = __fdiv_rn(r.hi, b.hi);
-  return add(q, F2{q3, 0.0f});
+  return fast_two_sum(q1, q2);
 }
 
 __device__ __forceinline__ F2 scale(F2 a, int n) { return {ldexpf(a.hi, n), ldexpf(a.lo, n)}; }
@@ -109,11 +109,21 @@ __device__ __forceinline__ F2 exp_reduced(F2 d, int& n_out) {
   // r = d - nf*ln2; nf*ln2 formed as a float-float product
   const F2 t = add(two_prod(nf, kLn2Hi), F2{__fmul_rn(nf, kLn2Lo), 0.0f});
   const F2 r = add(d, F2{-t.hi, -t.lo});
-  F2 p{kInvFactHi[kTaylorDegree], kInvFactLo[kTaylorDegree]};
+  auto c = [](int i) { return F2{kInvFactHi[i], kInvFactLo[i]}; };
+  const F2 p01 = add(F2{1.0f, 0.0f}, r);  // 1/0! + r/1!
+  const F2 p23 = add(c(2), mul(c(3), r));
+  const F2 p45 = add(c(4), mul(c(5), r));
+  const F2 p67 = add(c(6), mul(c(7), r));
+  const F2 r2 = mul(r, r);
+  const F2 r4 = mul(r2, r2);
+  const F2 h = add(add(p01, mul(r2, p23)), mul(r4, add(p45, mul(r2, p67))));
+  // degrees 8..13 in fp32: |r^8/8!| < 2^-27, so fp32 rounding stays below 2^-50
+  const float x = r.hi, x2 = __fmul_rn(x, x), x4 = __fmul_rn(x2, x2), x8 = __fmul_rn(x4, x4);
+  float tail = kInvFactHi[kTaylorDegree];
 #pragma unroll
-  for (int i = kTaylorDegree - 1; i >= 0; --i) p = add(mul(p, r), F2{kInvFactHi[i], kInvFactLo[i]});
+  for (int i = kTaylorDegree - 1; i >= 8; --i) tail = __fmaf_rn(tail, x, kInvFactHi[i]);
   n_out = (int)nf;
-  return p;
+  return add(h, F2{__fmul_rn(x8, tail), 0.0f});
 }
 
 }  // namespace ff

@@ -118,8 +118,10 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(const LayoutArgs p) {
   layout_tables(p, smem);
 }
 
+// Two CTAs per SM (64 registers) where the route fits in them; with 16 or 32
+// logits per lane one CTA per SM, so that the keys stay in registers.
 template <bool ROUTE, int EPL>
-__global__ void __launch_bounds__(kLayoutThreads) k_layout(const LayoutArgs p) {
+__global__ void __launch_bounds__(kLayoutThreads, EPL >= 16 ? 1 : 2) k_layout(const LayoutArgs p) {
   extern __shared__ int smem[];
   layout_chunk<ROUTE, EPL>(p, blockIdx.x, smem);
 }

@@ -191,6 +191,45 @@ def test_layout_route_only_entry_point(gpu):
     assert f32_ulp_diff(w.cpu().numpy(), ow).max() <= 1
 
 
+ROUTE_CASES = [(256, 8), (64, 2), (8, 2), (1024, 32), (32, 1), (128, 5), (512, 16), (16, 8)]
+
+
+@pytest.mark.parametrize("E,k", ROUTE_CASES, ids=[f"E{e}k{k}" for e, k in ROUTE_CASES])
+def test_route_ties_gaps_and_chunkings(gpu, E, k):
+    """Routing on logits with many exact ties (integers in [-3, 3] and rows of
+    one repeated value: the lower expert wins), with large gaps (N(0, 40):
+    weights far below 1, some under the float-float range) and N(0, 1), through
+    the route-only kernel and the fused route+layout with one token per warp
+    (small chunks) and several (large chunks): ids exact, weights within
+    1 fp32 ulp of the double softmax."""
+    import torch
+    import oracle
+    from combine_top_histogram_gb300 import MoeLayer
+    from combine_top_histogram_gb300 import binding as B
+    from harness import f32_ulp_diff
+    rng = np.random.default_rng(E * 100 + k)
+    for Tr in (6, 2600):  # one token per routing warp / several per warp (T > 32 * SMs)
+        P = 2
+        T = P * Tr
+        z = np.concatenate([
+            rng.integers(-3, 4, (T // 3, E)).astype(np.float32),
+            (rng.standard_normal((T // 3, E)) * 40).astype(np.float32),
+            rng.standard_normal((T - 2 * (T // 3), E)).astype(np.float32)])
+        z[0, :] = 0.5  # every logit equal
+        oi, ow = oracle.route_topk(z, k)
+        zt = torch.from_numpy(z).cuda()
+        layer = MoeLayer(P, Tr, E, k, 128)
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        B.moe_route_topk(layer.handle, zt, ids, w)
+        layer.route_layout(zt)
+        torch.cuda.synchronize()
+        for gi, gw in ((ids, w), (layer.ids, layer.w)):
+            assert np.array_equal(gi.cpu().numpy(), oi), (Tr, E, k)
+            assert f32_ulp_diff(gw.cpu().numpy(), ow).max() <= 1, (Tr, E, k)
+        assert oi[0].tolist() == list(range(k))
+
+
 def test_layout_tables_without_dispatch(gpu):
     """The per-source tables (cnt, kept counts, C, send and receive offsets)
     are left to the dispatch launch; moe_layout_tables builds them alone. With
