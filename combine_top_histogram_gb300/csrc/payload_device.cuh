@@ -73,6 +73,64 @@ __device__ __forceinline__ uint2 quant8(const uint4 x, float s, float m) {
   return make_uint2(out[0], out[1]);
 }
 
+// 32 bytes (16 bf16 values) in one 256-bit load, last-use hint; p 32-byte aligned.
+__device__ __forceinline__ void ld_stream32(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.lu.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                 "=r"(b.w)
+               : "l"(p));
+}
+
+// Two fp32 lanes in one 64-bit register (first value in the low half) and the
+// packed round-to-nearest multiply and fused multiply-add, each lane rounded
+// exactly as the scalar operation.
+__device__ __forceinline__ unsigned long long f32x2(float lo, float hi) {
+  return ((unsigned long long)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ unsigned long long mul_f32x2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// quant8 for 16 values (two 16-byte vectors a, b of one block): the same
+// quotient and codes, the FMA steps of div_by_scale on two values per
+// instruction. Returns the 16 codes in memory order.
+__device__ __forceinline__ uint4 quant16(const uint4 a, const uint4 b, float s, float m) {
+  if (m == 0.0f) return make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t out[4] = {0u, 0u, 0u, 0u};
+  if (__float_as_uint(m) - 0x1F800000u < 0x7F800000u - 0x1F800000u) {
+    const float yh = __frcp_rn(s);
+    const float yl = __fmul_rn(__fmaf_rn(-s, yh, 1.0f), yh);
+    const unsigned long long yh2 = f32x2(yh, yh), yl2 = f32x2(yl, yl), ns2 = f32x2(-s, -s);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const unsigned long long x2 = f32x2(bf16_lo(w[q]), bf16_hi(w[q]));
+      const unsigned long long q0 = fma_f32x2(x2, yh2, mul_f32x2(x2, yl2));
+      const unsigned long long r = fma_f32x2(ns2, q0, x2);
+      const unsigned long long qq = fma_f32x2(r, yh2, q0) | (x2 & 0x8000000080000000ull);
+      const float2 f = make_float2(__uint_as_float((uint32_t)qq), __uint_as_float((uint32_t)(qq >> 32)));
+      const uint32_t c = (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      out[q >> 1] |= c << (16 * (q & 1));
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float2 qq = make_float2(__fdiv_rn(bf16_lo(w[q]), s), __fdiv_rn(bf16_hi(w[q]), s));
+      const uint32_t c = (uint32_t)__nv_cvt_float2_to_fp8x2(qq, __NV_SATFINITE, __NV_E4M3);
+      out[q >> 1] |= c << (16 * (q & 1));
+    }
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 __device__ __forceinline__ float amax8(const uint4 x) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
   float m = 0.f;

@@ -25,15 +25,22 @@ def to_np_bits(t):
 
 def run_gpu(wl: W.Workload, inp: W.Inputs, ids=None, layer=None, stream=None,
             copy_rows: bool = True, two_stage: bool = False, fused: bool = False,
-            pipelined: int = 0, allgather: bool = False):
+            pipelined: int = 0, allgather: bool = False, x_offset16: bool = False):
     """The path on the GPU through the C ABI; returns host copies of everything
-    (copy_rows=False leaves the row buffers on the device, in res["layer"])."""
+    (copy_rows=False leaves the row buffers on the device, in res["layer"]).
+    x_offset16: x starts 16 bytes past a 256-byte boundary (16-byte aligned,
+    not 32-byte aligned), which selects the dispatch's 16-byte-load kernels."""
     import torch
     from combine_top_histogram_gb300 import MoeLayer
     dev = torch.device("cuda:0")
     if layer is None:
         layer = MoeLayer(wl.P, wl.Tr, wl.E, wl.k, wl.H, wl.dispatch_dtype, wl.cap, "cuda:0")
     x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    if x_offset16:
+        buf = torch.empty(x.numel() + 8, dtype=torch.bfloat16, device=dev)
+        buf[8:].copy_(x.reshape(-1))
+        x = buf[8:].view(x.shape)
+        assert x.data_ptr() % 32 == 16
     c = torch.from_numpy(inp.expert_scale).to(dev) if inp.expert_scale is not None else None
     if pipelined:
         if ids is None and inp.logits is not None:

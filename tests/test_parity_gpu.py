@@ -161,6 +161,17 @@ def test_fp8_capacity_parity(gpu, cap):
     _check(wl, inp)
 
 
+@pytest.mark.parametrize("name", ["uniform_fp8", "prefill_cap"])
+def test_fp8_dispatch_with_x_only_16_byte_aligned(gpu, name):
+    """x 16- but not 32-byte aligned: the FP8 dispatch takes its 16-byte-load
+    kernel instead of the 32-byte one; both must match the oracle exactly."""
+    wl = {"uniform_fp8": W.UNIFORM_FP8.scaled("u16", Tr=300, H=1024),
+          "prefill_cap": W.PREFILL.scaled("p16", Tr=40, H=7168, cap=30)}[name]
+    inp = W.make_inputs(wl)
+    g = run_gpu(wl, inp, x_offset16=True)
+    compare(wl, g, run_oracle(wl, inp), routed=inp.logits is not None)
+
+
 def test_fp8_extreme_values(gpu):
     """Blocks with tiny, huge and mixed magnitudes (subnormal e4m3 codes,
     saturation at the amax element, negative zero after rounding)."""
