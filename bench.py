@@ -160,9 +160,15 @@ def hbm_peak():
 
 
 def source_sha(kernel: str) -> str:
-    src = os.path.join(ROOT, "combine_top_histogram_gb300", "csrc", KERNEL_SOURCES[kernel])
-    with open(src, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Fingerprint of a kernel's source: its .cu file and every header of the
+    CUDA sources (a header change may change any kernel)."""
+    csrc = os.path.join(ROOT, "combine_top_histogram_gb300", "csrc")
+    files = [KERNEL_SOURCES[kernel]] + sorted(f for f in os.listdir(csrc) if f.endswith(".cuh"))
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def committed_traffic(kernel: str, workload: str):
