@@ -50,14 +50,18 @@ __device__ __forceinline__ void fma8(float* acc, float w, const uint4 y) {
 // K == 0: any k <= MOE_MAX_TOPK, loads issued in groups of 8.
 template <int K, int VPT>
 __global__ void __launch_bounds__(kCombineThreads) k_combine(const CombineArgs p) {
-  __shared__ int rows_s[MOE_MAX_TOPK];
-  __shared__ float w_s[MOE_MAX_TOPK];
+  // the token's k rows and weights; two buffers, alternating per token
+  __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  __shared__ float w_buf[2][MOE_MAX_TOPK];
+  int par = 0;
   const int nvec = p.H >> 3;
   const int tid = threadIdx.x;
   const int k = K > 0 ? K : p.k;
   pdl_wait();  // y (and inv, when dispatch ran just before) come from earlier kernels
   pdl_trigger();
   for (long long g = p.g0 + blockIdx.x; g < p.T; g += gridDim.x) {
+    int* rows_s = rows_buf[par];
+    float* w_s = w_buf[par];
     if (tid < k) {
       rows_s[tid] = __ldg(p.inv + g * k + tid);
       w_s[tid] = __ldg(p.w + g * k + tid);
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const CombineArgs p
         dst[v] = o;
       }
     }
-    __syncthreads();
+    par ^= 1;  // token n+2 rewrites this buffer only after token n+1's barrier
   }
 }
 

@@ -90,7 +90,9 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
 
 template <int VPT>
 __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const DispatchArgs p) {
-  __shared__ int rows_s[MOE_MAX_TOPK];
+  // the k receive rows of the current token; two buffers, alternating per token
+  __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  int par = 0;
   const int nvec = p.H >> 3;  // 16-byte vectors per row
   const int tid = threadIdx.x;
   bool waited = false;
@@ -100,6 +102,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
   }
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
+    int* rows_s = rows_buf[par];
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
         }
       }
     }
-    __syncthreads();
+    par ^= 1;  // token n+2 rewrites this buffer only after token n+1's barrier
   }
 }
 
@@ -138,7 +141,9 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
 // amax is a 4-step xor-shuffle reduction inside each half-warp.
 template <int VPT>
 __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const DispatchArgs p) {
-  __shared__ int rows_s[MOE_MAX_TOPK];
+  // the k receive rows of the current token; two buffers, alternating per token
+  __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  int par = 0;
   const int nvec = p.H >> 3;
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
@@ -149,6 +154,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
   }
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
+    int* rows_s = rows_buf[par];
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -191,7 +197,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
         }
       }
     }
-    __syncthreads();
+    par ^= 1;  // token n+2 rewrites this buffer only after token n+1's barrier
   }
 }
 
@@ -203,7 +209,9 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
 // the next, so only the loaded rows stay in registers.
 template <int CPT>
 __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const DispatchArgs p) {
-  __shared__ int rows_s[MOE_MAX_TOPK];
+  // the k receive rows of the current token; two buffers, alternating per token
+  __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  int par = 0;
   const int nch = p.H >> 4;  // 32-byte chunks (16 values) per row
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
@@ -214,6 +222,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
   }
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
+    int* rows_s = rows_buf[par];
     const uint16_t* src = p.x + g * p.H;
     for (int c0 = 0; c0 < nch; c0 += CPT * kDispatchThreads) {
       uint4 va[CPT], vb[CPT];
@@ -254,7 +263,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
         }
       }
     }
-    __syncthreads();
+    par ^= 1;  // token n+2 rewrites this buffer only after token n+1's barrier
   }
 }
 
