@@ -43,7 +43,7 @@ int validate(const moe_config_t* c) {
 
 struct Plan {
   int tpc_route, cps_route, tpc_ids, cps_ids, nchunks_max;
-  size_t off_ctrl, off_totals, off_n_raw, off_n_kept, off_eoff, off_cnt, off_kept, off_C,
+  size_t off_ctrl, off_acc, off_totals, off_n_raw, off_n_kept, off_eoff, off_cnt, off_kept, off_C,
       off_send, off_recv, off_rank, off_hist, off_pre, off_acode, off_inv, off_spos, off_sbase,
       bytes;
 };
@@ -83,6 +83,7 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
     return o;
   };
   p.off_ctrl = take(64);
+  p.off_acc = take((size_t)2 * E * 4);
   p.off_totals = take(4 * sizeof(int32_t));
   p.off_n_raw = take((size_t)E * 4);
   p.off_n_kept = take((size_t)E * 4);
@@ -140,6 +141,8 @@ moe::LayoutArgs layout_args(moe_handle_t h, bool route) {
   a.cap = h->cfg.expert_capacity;
   a.Na = h->Na;
   a.defer_tables = 1;
+  a.acc_add = h->acc + (h->acc_gen & 1ull) * a.E;
+  a.acc_zero = h->acc + ((h->acc_gen + 1ull) & 1ull) * a.E;
   return a;
 }
 
@@ -240,7 +243,9 @@ int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
   h->send_pos = reinterpret_cast<int32_t*>(ws + p.off_spos);
   h->src_base = reinterpret_cast<int32_t*>(ws + p.off_sbase);
   h->wait_limit = 1ll << 22;  // ~0.3 s of 64 ns polls
-  if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess) {
+  h->acc = reinterpret_cast<int32_t*>(ws + p.off_acc);
+  if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess ||
+      cudaMemset(ws + p.off_acc, 0, (size_t)2 * cfg->num_experts * 4) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
   }
@@ -261,13 +266,23 @@ int moe_route_topk(moe_handle_t h, const float* logits, int32_t* ids, float* w, 
 
 static int run_layout(moe_handle_t h, bool route, const int32_t* ids_in, const float* logits,
                       int32_t* ids_out, float* w_out, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (h->acc_dirty) {  // a failed launch may have left partial totals
+    if (cudaMemsetAsync(h->acc, 0, (size_t)2 * h->cfg.num_experts * 4, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    h->acc_dirty = 0;
+  }
   moe::LayoutArgs a = layout_args(h, route);
   a.ids_in = ids_in;
   a.logits = logits;
   a.ids_out = ids_out;
   a.w_out = w_out;
-  const int rc = cuda_rc(moe::launch_layout(a, route, h->num_sms, static_cast<cudaStream_t>(stream)));
-  if (rc != MOE_OK) return rc;
+  const int rc = cuda_rc(moe::launch_layout(a, route, h->num_sms, st));
+  if (rc != MOE_OK) {
+    h->acc_dirty = 1;
+    return rc;
+  }
+  h->acc_gen += 1;
   h->cur_tpc = a.tpc;
   h->cur_cps = a.cps;
   h->layout_gen += 1;
@@ -516,6 +531,8 @@ int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids,
   moe::FusedArgs f{};
   f.lay = layout_args(h, route);
   f.lay.defer_tables = 0;  // the persistent kernel builds every table itself
+  f.lay.acc_add = nullptr;
+  f.lay.acc_zero = nullptr;
   f.lay.ids_in = ids;
   f.lay.logits = logits;
   f.lay.ids_out = ids;

@@ -57,6 +57,13 @@ struct LayoutArgs {
   // offsets, rank bases, totals); the per-source tables are left to
   // source_tables (dispatch CTAs or k_tables). 0: it writes every table.
   int defer_tables;
+  // Per-expert totals accumulated by the layout kernel (one integer add per
+  // chunk and expert), or null. With them every scan CTA derives the expert
+  // offsets itself, so the scan needs no arrival counter and no last CTA
+  // (requires defer_tables). acc_zero is the other of two alternating
+  // buffers: the scan clears it for the next layout.
+  int32_t* acc_add;
+  int32_t* acc_zero;
 };
 
 // Per-source tables of the layout, one source rank s per CTA (source_tables):
@@ -227,5 +234,8 @@ struct moe_handle {
       *recv_offset, *rank_base, *hist, *src_pre, *acode, *inv, *send_pos, *src_base;
   unsigned long long layout_gen, dispatch_gen;
   int tables_pending;       // per-source tables of the last layout not yet built
+  int32_t* acc;             // [2][E] per-expert totals, alternating per layout
+  unsigned long long acc_gen;
+  int acc_dirty;            // a failed layout launch may have left partial sums
   long long wait_limit;     // bounded device waits (persistent path)
 };

@@ -52,9 +52,43 @@ namespace {
 // to kScanRun chunks, issuing all its loads at once, so a column costs one
 // L2 round trip and one warp shuffle scan of the lanes' sums; longer columns
 // take further passes. The scan also records the prefix at each source
-// rank's first chunk and the expert's totals. The last CTA to arrive builds
-// the tables.
+// rank's first chunk and the expert's totals.
+//
+// With per-expert totals accumulated by the layout kernel (p.acc_add), one
+// extra CTA (the last) turns them into the expert offsets, rank bases and
+// totals and clears the other accumulator for the next layout, while the
+// other CTAs scan columns: no CTA waits for another. Without them, the last
+// CTA to arrive (threadfence + arrival counter) builds the tables.
 constexpr int kScanRun = 8;
+
+__device__ void offsets_from_totals(const LayoutArgs& p, int* smem) {
+  const int E = p.E, tid = threadIdx.x, NT = blockDim.x;
+  int* sk = smem;        // [E] kept counts -> expert offsets
+  int* tmp = sk + E;     // [32]
+  int* red = tmp + 32;   // [2] dropped, raw total
+  if (tid < 2) red[tid] = 0;
+  __syncthreads();
+  int dr = 0, rw = 0;
+  for (int e = tid; e < E; e += NT) {
+    const int raw = __ldcg(p.acc_add + e);
+    const int kept = (p.cap > 0 && raw > p.cap) ? p.cap : raw;
+    sk[e] = kept;
+    rw += raw;
+    dr += raw - kept;
+    p.acc_zero[e] = 0;
+  }
+  if (dr) atomicAdd(&red[0], dr);
+  if (rw) atomicAdd(&red[1], rw);
+  const int total = cta_exclusive_scan(sk, E, tmp);
+  for (int e = tid; e <= E; e += NT) p.expert_offset[e] = e < E ? sk[e] : total;
+  for (int d = tid; d <= p.P; d += NT) p.rank_base[d] = d < p.P ? sk[d * p.L] : total;
+  if (tid == 0) {
+    p.totals[0] = total;
+    p.totals[1] = red[0];
+    p.totals[2] = (int)(p.Na - (long long)red[1]);
+    p.totals[3] = 0;
+  }
+}
 
 __global__ void __launch_bounds__(kScanThreads) k_scan(const LayoutArgs p) {
   extern __shared__ int smem[];
@@ -62,6 +96,11 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(const LayoutArgs p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x * (kScanThreads / 32) + warp;
   pdl_wait();
+  if (p.acc_add && blockIdx.x == gridDim.x - 1) {
+    offsets_from_totals(p, smem);
+    pdl_trigger();
+    return;
+  }
   if (e < p.E) {
     int* col = p.hist + (long long)e * p.nchunks;
     const int n = p.nchunks;
@@ -104,6 +143,10 @@ __global__ void __launch_bounds__(kScanThreads) k_scan(const LayoutArgs p) {
       p.n_raw[e] = carry;
       p.n_kept[e] = (p.cap > 0 && carry > p.cap) ? p.cap : carry;
     }
+  }
+  if (p.acc_add) {
+    pdl_trigger();
+    return;
   }
   __threadfence();
   __syncthreads();
@@ -216,7 +259,7 @@ cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cuda
   cudaError_t err = launch_pdl(reinterpret_cast<void (*)(const LayoutArgs)>(fn), dim3(a.nchunks),
                                dim3(kLayoutThreads), smem, st, a);
   if (err != cudaSuccess) return err;
-  const int scan_blocks = (a.E + kScanThreads / 32 - 1) / (kScanThreads / 32);
+  const int scan_blocks = (a.E + kScanThreads / 32 - 1) / (kScanThreads / 32) + (a.acc_add ? 1 : 0);
   return launch_pdl(k_scan, dim3(scan_blocks), dim3(kScanThreads), scan_smem_bytes(a.E, a.P), st,
                     a);
 }

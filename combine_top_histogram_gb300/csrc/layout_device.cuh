@@ -316,6 +316,7 @@ __device__ __forceinline__ void layout_chunk(const LayoutArgs& p, int b, int* sm
       run += v;
     }
     p.hist[(long long)e * p.nchunks + b] = run;  // transposed: [E][nchunks]
+    if (p.acc_add && run) atomicAdd(p.acc_add + e, run);  // the expert's total
   }
   __syncthreads();
   // Pass 2: stable rank of every assignment within the chunk and expert.
