@@ -64,8 +64,12 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   if (tpc > Tr) tpc = Tr;
   p.tpc_ids = tpc;
   p.cps_ids = ceil_div(Tr, tpc);
+  // Routing chunks: about two per SM, and at least 8 tokens (the 16 warps of
+  // a chunk route one token each at most; the route is issue-bound, so fewer
+  // routing warps per SM finish sooner, while more chunks lengthen the column
+  // scan: 8 measured best at decode).
   int tr = (int)((T + 2ll * num_sms - 1) / (2ll * num_sms));
-  if (tr < moe::kLayoutWarps) tr = moe::kLayoutWarps;  // at least one token per warp
+  if (tr < 8) tr = 8;
   if (tr > 2048 / k) tr = 2048 / k;
   if (tr < 1) tr = 1;
   if (tr > max_tpc) tr = max_tpc;
