@@ -27,12 +27,17 @@
 //     re-walks the sub-range and gives each assignment its stable rank = warp
 //     base + lanes of the same expert below it. No atomics decide any
 //     position, so the layout is deterministic.
-//   * The chunk histogram goes to global memory transposed, [E][nchunks]. A
-//     second kernel (k_scan) scans it with one warp per expert column, and its
-//     last CTA to arrive (threadfence + arrival counter, no spinning) derives
-//     n_e, expert_offset, cnt[s][e], C[s][d], send_offset, recv_offset and
-//     rank_base, applying the capacity clamp. Both kernels use programmatic
-//     dependent launch, so the scan's CTAs are resident before the counts land.
+//   * The chunk histogram goes to global memory transposed, [E][nchunks], and
+//     each chunk adds its per-expert counts into per-expert totals (integer
+//     adds: order-free). A second kernel (k_scan) scans the histogram with one
+//     warp per expert column; one extra CTA turns the totals into n_e,
+//     expert_offset, rank_base and the layer totals with the capacity clamp.
+//     The per-source tables (cnt, kept counts, C, send and receive offsets)
+//     are built beside the copy by the dispatch launch (tables_device.cuh).
+//     Without the totals (persistent and no-allocation paths) the scan's last
+//     CTA to arrive (threadfence + arrival counter, no spinning) derives them.
+//     Both kernels use programmatic dependent launch, so the scan's CTAs are
+//     resident before the counts land.
 //   * The device pieces shared with the persistent path live in
 //     layout_device.cuh.
 #include <cuda_runtime.h>
