@@ -46,10 +46,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--dispatch", default="separate",
-                    choices=["separate", "fused", "two_stage", "allgather"],
+                    choices=["separate", "fused", "two_stage", "allgather", "fixed_slots"],
                     help="separate: layout kernels then the dispatch kernel; fused: one "
                          "persistent launch; two_stage: the pack + all-to-all-v comparator; "
-                         "allgather: the all-tokens-to-every-rank comparator")
+                         "allgather: the all-tokens-to-every-rank comparator; fixed_slots: "
+                         "fixed per-(source, expert) receive regions (no capacity)")
     ap.add_argument("--pipeline", type=int, default=0,
                     help="also time the token-chunked two-stream pipeline with N chunks")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
@@ -306,6 +307,8 @@ def run_ours(args, wl, rank, world, local):
             layer.dispatch_two_stage(x, w, stream)
         elif args.dispatch == "allgather":
             layer.dispatch_allgather(x, w, stream)
+        elif args.dispatch == "fixed_slots":
+            layer.dispatch_fixed_slots(x, w, stream)
         elif args.dispatch == "separate":
             layer.dispatch(x, w, stream)
 
@@ -469,6 +472,8 @@ def run_ours(args, wl, rank, world, local):
         dkey = "two_stage(k_send_pos+" + dkey + "+k_a2av)"
     if args.dispatch == "allgather":
         dkey = "allgather(k_allgather+k_allgather_filter)"
+    if args.dispatch == "fixed_slots":
+        dkey = "fixed_slots(" + dkey + ")"
     if args.dispatch == "fused":
         lkey = "k_fused(route+layout+dispatch)"
         means = {lkey: statistics.fmean([a + b for a, b in zip(lay_ms, dis_ms)]),

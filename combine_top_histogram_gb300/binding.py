@@ -33,7 +33,8 @@ EXPORTED_SYMBOLS = (
     "moe_dispatch_layout_noalloc", "moe_copy_h2d_async", "moe_copy_d2h_async",
     "moe_dispatch_two_stage", "moe_layout_dispatch_fused", "moe_set_wait_limit",
     "moe_dispatch_tokens", "moe_expert_standin_tokens", "moe_combine_tokens",
-    "moe_dispatch_allgather", "moe_layout_tables",
+    "moe_dispatch_allgather", "moe_layout_tables", "moe_dispatch_fixed_slots",
+    "moe_fixed_slot_rows",
 )
 
 
@@ -97,6 +98,10 @@ def load_library():
         lib.moe_dispatch_layout.argtypes = [vp, vp, vp]
         lib.moe_route_dispatch_layout.restype = i32
         lib.moe_route_dispatch_layout.argtypes = [vp, vp, vp, vp, vp]
+        lib.moe_dispatch_fixed_slots.restype = i32
+        lib.moe_dispatch_fixed_slots.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(moe_recv_meta_t), vp]
+        lib.moe_fixed_slot_rows.restype = ctypes.c_int64
+        lib.moe_fixed_slot_rows.argtypes = [cfgp]
         lib.moe_layout_tables.restype = i32
         lib.moe_layout_tables.argtypes = [vp, vp]
         lib.moe_get_layout.restype = i32
@@ -229,6 +234,19 @@ def moe_dispatch_layout(h: Handle, ids, stream=None) -> None:
 def moe_route_dispatch_layout(h: Handle, logits, ids, w, stream=None) -> None:
     _check("moe_route_dispatch_layout", load_library().moe_route_dispatch_layout(
         h.ptr, _ptr(logits), _ptr(ids), _ptr(w), _stream(stream)))
+
+
+def moe_fixed_slot_rows(cfg) -> int:
+    return int(load_library().moe_fixed_slot_rows(ctypes.byref(cfg)))
+
+
+def moe_dispatch_fixed_slots(h: Handle, x, w, slot_x, slot_scale, meta: dict, stream=None) -> None:
+    """Dispatch into fixed per-(source, expert) slot regions (see the header)."""
+    m = moe_recv_meta_t(*(_ptr(meta[n]) for n in (
+        "local_expert", "src_rank", "src_token", "slot", "weight")))
+    _check("moe_dispatch_fixed_slots", load_library().moe_dispatch_fixed_slots(
+        h.ptr, _ptr(x), _ptr(w), _ptr(slot_x), _ptr(slot_scale), ctypes.byref(m),
+        _stream(stream)))
 
 
 def moe_layout_tables(h: Handle, stream=None) -> None:

@@ -174,6 +174,15 @@ int ensure_tables(moe_handle_t h, cudaStream_t st) {
   return rc;
 }
 
+// Rows of the fixed per-(source, expert) slot layout: E regions of P*T_r rows;
+// 0 when a capacity is set (the kept set would depend on every source) or the
+// rows would not fit int32 indices.
+long long fixed_slot_rows(const moe_config_t* c) {
+  const long long rows = (long long)c->num_experts * c->num_ranks * c->tokens_per_rank;
+  if (c->expert_capacity > 0 || rows >= (1ll << 31)) return 0;
+  return rows;
+}
+
 }  // namespace
 
 extern "C" {
@@ -183,6 +192,11 @@ size_t moe_workspace_bytes(const moe_config_t* cfg) {
   int dev = 0, sms = 0;
   if (query_sms(&dev, &sms) != MOE_OK) sms = 152;
   return make_plan(cfg, sms).bytes;
+}
+
+int64_t moe_fixed_slot_rows(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  return fixed_slot_rows(cfg);
 }
 
 int64_t moe_recv_rows_max(const moe_config_t* cfg) {
@@ -329,7 +343,7 @@ int moe_get_layout(moe_handle_t h, moe_layout_view_t* out) {
 
 static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void* x,
                           const float* w, void* recv_x, float* recv_scale,
-                          const moe_recv_meta_t* meta, void* stream) {
+                          const moe_recv_meta_t* meta, void* stream, bool fixed = false) {
   if (!h || !x || !w || !recv_x || !meta) return MOE_ERR_INVALID_ARG;
   if (!meta->local_expert || !meta->src_rank || !meta->src_token || !meta->slot || !meta->weight)
     return MOE_ERR_INVALID_ARG;
@@ -366,12 +380,25 @@ static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void
     a.tab = tables_args(h);
     a.tab_ctas = h->cfg.num_ranks;
   }
+  a.P = h->cfg.num_ranks;
+  if (fixed) {
+    a.src_pre = h->src_pre;
+    a.slot_Tr = h->cfg.tokens_per_rank;
+  }
   const int rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
   if (rc == MOE_OK) {
     h->dispatch_gen = h->layout_gen;
     h->tables_pending = 0;
+    h->fixed_rows = fixed ? 1 : 0;
   }
   return rc;
+}
+
+int moe_dispatch_fixed_slots(moe_handle_t h, const void* x, const float* w, void* slot_x,
+                             float* slot_scale, const moe_recv_meta_t* meta, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (fixed_slot_rows(&h->cfg) == 0) return MOE_ERR_UNSUPPORTED;
+  return dispatch_range(h, 0, h->T, x, w, slot_x, slot_scale, meta, stream, true);
 }
 
 int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* send_x,
@@ -434,7 +461,10 @@ int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* 
   c.E = h->cfg.num_experts;
   c.nblk = h->cfg.hidden / 128;
   rc = cuda_rc(moe::launch_a2av(c, h->num_sms, st));
-  if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
+  if (rc == MOE_OK) {
+    h->dispatch_gen = h->layout_gen;
+    h->fixed_rows = 0;
+  }
   return rc;
 }
 
@@ -494,7 +524,10 @@ int moe_dispatch_allgather(moe_handle_t h, const void* x, const float* w, void* 
   int rc = ensure_tables(h, static_cast<cudaStream_t>(stream));
   if (rc != MOE_OK) return rc;
   rc = cuda_rc(moe::launch_allgather(g, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
-  if (rc == MOE_OK) h->dispatch_gen = h->layout_gen;
+  if (rc == MOE_OK) {
+    h->dispatch_gen = h->layout_gen;
+    h->fixed_rows = 0;
+  }
   return rc;
 }
 
@@ -579,6 +612,7 @@ int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids,
   h->layout_gen += 1;
   h->dispatch_gen = h->layout_gen;
   h->tables_pending = 0;
+  h->fixed_rows = 0;
   return MOE_OK;
 }
 
@@ -599,6 +633,14 @@ int moe_expert_standin(moe_handle_t h, const void* recv_x, const float* recv_sca
   a.E = h->cfg.num_experts;
   a.H = h->cfg.hidden;
   a.fp8 = fp8 ? 1 : 0;
+  if (h->fixed_rows) {  // the filled rows of every slot region, found through inv
+    a.inv = h->inv;
+    a.a0 = 0;
+    a.a1 = h->Na;
+    a.k = h->cfg.top_k;
+    a.slot_rows = (long long)h->cfg.num_ranks * h->cfg.tokens_per_rank;
+    return cuda_rc(moe::launch_standin_tokens(a, h->num_sms, static_cast<cudaStream_t>(stream)));
+  }
   return cuda_rc(moe::launch_standin(a, h->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -654,6 +696,7 @@ int moe_expert_standin_tokens(moe_handle_t h, int64_t token_begin, int64_t token
   a.E = h->cfg.num_experts;
   a.H = h->cfg.hidden;
   a.fp8 = fp8 ? 1 : 0;
+  if (h->fixed_rows) a.slot_rows = (long long)h->cfg.num_ranks * h->cfg.tokens_per_rank;
   return cuda_rc(moe::launch_standin_tokens(a, h->num_sms, static_cast<cudaStream_t>(stream)));
 }
 

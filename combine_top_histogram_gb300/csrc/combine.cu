@@ -192,10 +192,14 @@ __global__ void __launch_bounds__(128) k_standin_tokens(const StandinArgs p) {
       r_s = r;
       if (r >= 0) {
         int lo = 0, hi = p.E - 1;  // largest e with expert_offset[e] <= r
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (__ldg(p.expert_offset + mid) <= r) lo = mid;
-          else hi = mid - 1;
+        if (p.slot_rows > 0) {     // fixed slots: expert regions of slot_rows rows
+          lo = (int)(r / p.slot_rows);
+        } else {
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(p.expert_offset + mid) <= r) lo = mid;
+            else hi = mid - 1;
+          }
         }
         c_s = p.expert_scale ? __ldg(p.expert_scale + lo) : 1.0f;
       }

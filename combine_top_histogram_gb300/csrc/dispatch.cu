@@ -70,7 +70,9 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
     const int b = s * p.cps + t / p.tpc;
     const int pos = __ldg(p.hist + (long long)e * p.nchunks + b) + code_rank(code);
     if (p.cap <= 0 || pos < p.cap) {
-      r = __ldg(p.expert_offset + e) + pos;
+      r = p.slot_Tr > 0
+              ? (e * p.P + s) * p.slot_Tr + (pos - __ldg(p.src_pre + (long long)s * p.E + e))
+              : __ldg(p.expert_offset + e) + pos;
       p.m_local_expert[r] = e % p.L;
       p.m_src_rank[r] = s;
       p.m_src_token[r] = t;

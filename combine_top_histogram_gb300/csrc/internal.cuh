@@ -106,6 +106,11 @@ struct DispatchArgs {
   // source each) while the others copy tokens.
   TablesArgs tab;
   int tab_ctas;
+  // Fixed per-(source, expert) receive slots when slot_Tr > 0: assignment
+  // (s, t, j) -> e goes to row (e*P + s)*slot_Tr + q, q its rank among s's
+  // assignments to e; src_pre gives the prefix at s's first chunk.
+  const int32_t* src_pre;
+  int slot_Tr, P;
 };
 
 // Persistent single-launch route/layout/dispatch (fused.cu).
@@ -162,6 +167,7 @@ struct StandinArgs {
   uint16_t* y;
   long long rows_max;
   int E, H, fp8;
+  long long slot_rows;     // fixed-slot layout: rows per expert region (P*T_r); 0 = compact
 };
 
 // Programmatic dependent launch: every kernel of the path is launched with
@@ -237,5 +243,6 @@ struct moe_handle {
   int32_t* acc;             // [2][E] per-expert totals, alternating per layout
   unsigned long long acc_gen;
   int acc_dirty;            // a failed layout launch may have left partial sums
+  int fixed_rows;           // the last dispatch wrote fixed per-(source, expert) slots
   long long wait_limit;     // bounded device waits (persistent path)
 };

@@ -42,6 +42,8 @@ class MoeLayer:
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.ids = torch.empty((T, k), dtype=torch.int32, device=dev)
         self.w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        self.slots = None  # fixed-slot buffers, allocated on first use
+        self.fixed = False  # the last dispatch wrote the fixed-slot layout
 
     # -- steps ---------------------------------------------------------------
     def route_layout(self, logits, stream=None):
@@ -58,6 +60,31 @@ class MoeLayer:
 
     def dispatch(self, x, w, stream=None):
         B.moe_dispatch(self.handle, x, w, self.recv_x, self.recv_scale, self.meta, stream)
+        self.fixed = False
+
+    def dispatch_fixed_slots(self, x, w, stream=None):
+        """The fixed-slot comparator: one region of T_r rows per (expert, source)
+        (E*T rows in all); expert() and combine() then use these buffers."""
+        import torch
+        if self.slots is None:
+            rows = B.moe_fixed_slot_rows(self.cfg)
+            if rows == 0:
+                raise ValueError("fixed slots need a configuration without capacity")
+            dev = self.out.device
+            sx = torch.empty((rows, self.H), dtype=torch.uint8 if self.fp8 else torch.bfloat16,
+                             device=dev)
+            self.slots = {
+                "x": sx,
+                "scale": (torch.empty((rows, self.H // 128), dtype=torch.float32, device=dev)
+                          if self.fp8 else None),
+                "meta": {n: torch.empty(rows, dtype=torch.float32 if n == "weight" else torch.int32,
+                                        device=dev)
+                         for n in ("local_expert", "src_rank", "src_token", "slot", "weight")},
+                "y": torch.empty((rows, self.H), dtype=torch.bfloat16, device=dev),
+            }
+        s = self.slots
+        B.moe_dispatch_fixed_slots(self.handle, x, w, s["x"], s["scale"], s["meta"], stream)
+        self.fixed = True
 
     def dispatch_two_stage(self, x, w, stream=None):
         """The two-stage comparator: pack into per-source send buffers, then a
@@ -69,6 +96,7 @@ class MoeLayer:
                                if self.recv_scale is not None else None)
         B.moe_dispatch_two_stage(self.handle, x, w, self.send_x, self.send_scale, self.recv_x,
                                  self.recv_scale, self.meta, stream)
+        self.fixed = False
 
     def dispatch_allgather(self, x, w, stream=None):
         """The AllGather comparator: all tokens to every rank, then a local filter."""
@@ -82,6 +110,7 @@ class MoeLayer:
                                    if self.fp8 else None)
         B.moe_dispatch_allgather(self.handle, x, w, self.gathered_x, self.gathered_scale,
                                  self.recv_x, self.recv_scale, self.meta, stream)
+        self.fixed = False
 
     def layout_dispatch_fused(self, x, ids=None, w=None, logits=None, stream=None):
         """One persistent launch: route (logits) or take ids/w, lay out, dispatch."""
@@ -89,16 +118,21 @@ class MoeLayer:
             ids, w = self.ids, self.w
         B.moe_layout_dispatch_fused(self.handle, logits, ids, w, x, self.recv_x, self.recv_scale,
                                     self.meta, stream)
+        self.fixed = False
 
     def expert(self, expert_scale=None, stream=None):
+        if self.fixed:
+            s = self.slots
+            B.moe_expert_standin(self.handle, s["x"], s["scale"], expert_scale, s["y"], stream)
+            return
         B.moe_expert_standin(self.handle, self.recv_x, self.recv_scale, expert_scale, self.y,
                              stream)
 
     def combine(self, w, stream=None):
-        B.moe_combine(self.handle, self.y, w, self.out, stream)
+        B.moe_combine(self.handle, self.slots["y"] if self.fixed else self.y, w, self.out, stream)
 
     def forward(self, x, ids=None, w=None, logits=None, expert_scale=None, stream=None,
-                two_stage=False, fused=False, allgather=False):
+                two_stage=False, fused=False, allgather=False, fixed_slots=False):
         """Whole layer; with logits the routed ids/weights land in self.ids / self.w.
         two_stage=True dispatches through the two-stage comparator."""
         if fused:
@@ -115,6 +149,8 @@ class MoeLayer:
             self.layout(ids, stream)
         if allgather:
             self.dispatch_allgather(x, w, stream)
+        elif fixed_slots:
+            self.dispatch_fixed_slots(x, w, stream)
         elif two_stage:
             self.dispatch_two_stage(x, w, stream)
         else:
@@ -133,6 +169,7 @@ class MoeLayer:
         if getattr(self, "_side", None) is None:
             self._side = torch.cuda.Stream(device=self.out.device)
         side = self._side
+        self.fixed = False
         if logits is not None:
             self.route_layout(logits, main)
             w = self.w

@@ -219,6 +219,28 @@ int moe_get_layout(moe_handle_t h, moe_layout_view_t *out);
 int moe_dispatch(moe_handle_t h, const void *x, const float *w, void *recv_x,
                  float *recv_scale, const moe_recv_meta_t *meta, void *stream);
 
+/* NEXT-row comparator, pplx-style fixed receive slots ("Efficient and
+ * portable MoE communication", "Dispatch" and "Combine": each rank keeps
+ * private storage per source, sized by the maximum tokens per rank). The
+ * receive buffer has one region of T_r rows per (expert e, source s), at row
+ * (e*P + s)*T_r; assignment (s, t, j) -> e lands at row (e*P + s)*T_r + q, q
+ * its rank among source s's assignments to e in (t, j) order. No row depends
+ * on another source's counts, so no scan across sources is needed, at the
+ * price of E*T rows of storage; region (e, s) holds src_expert_count[s][e]
+ * filled rows, the rest untouched. Needs a preceding layout call on a handle
+ * without capacity (MOE_ERR_UNSUPPORTED otherwise, or when the rows exceed
+ * int32). slot_x: moe_fixed_slot_rows(cfg) rows of H elements (bf16, or e4m3
+ * with fp32 slot_scale [rows, H/128]); meta arrays of that many rows. Same
+ * payload, scales and metadata per assignment as moe_dispatch; inv holds the
+ * slot rows, so moe_combine / moe_expert_standin (which then treats the slot
+ * layout) work unchanged on the slot buffers. */
+int moe_dispatch_fixed_slots(moe_handle_t h, const void *x, const float *w, void *slot_x,
+                             float *slot_scale, const moe_recv_meta_t *meta, void *stream);
+
+/* Rows of the fixed-slot receive buffer: E*P*T_r, 0 if *cfg is invalid, sets a
+ * capacity, or the rows exceed int32. */
+int64_t moe_fixed_slot_rows(const moe_config_t *cfg);
+
 /* NEXT-row comparator, the AllGather-style dispatcher ([EP] "Why not collect
  * all tokens with AllGather"): every rank first receives every token
  * (gathered_x: P*T rows, rank d's copy of token g at row d*T + g; FP8 rows are

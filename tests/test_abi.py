@@ -54,6 +54,15 @@ def test_host_only_sizing_and_validation(cuda_lib):
     assert cuda_lib.moe_handle_destroy(None) == 0
 
 
+def test_fixed_slot_rows_rule():
+    from combine_top_histogram_gb300 import binding as B
+    assert B.moe_fixed_slot_rows(B.make_config(8, 128, 256, 8, 7168)) == 256 * 8 * 128
+    assert B.moe_fixed_slot_rows(B.make_config(4, 2, 8, 2, 128)) == 8 * 4 * 2
+    assert B.moe_fixed_slot_rows(B.make_config(8, 128, 256, 8, 7168, cap=64)) == 0  # capacity
+    assert B.moe_fixed_slot_rows(B.make_config(32, 1 << 20, 256, 8, 128)) == 0  # > int32 rows
+    assert B.moe_fixed_slot_rows(B.make_config(3, 4, 8, 2, 64)) == 0  # invalid config
+
+
 def test_null_handles_are_rejected(cuda_lib):
     assert cuda_lib.moe_dispatch_layout(None, None, None) == -1
     assert cuda_lib.moe_combine(None, None, None, None, None) == -1
