@@ -19,6 +19,7 @@ MOE_BF16 = 0
 MOE_FP8_E4M3 = 1
 MOE_STATUS_BAD_EXPERT_ID = 0x1
 MOE_STATUS_TIMEOUT = 0x2
+MOE_STATUS_SLOT_OVERFLOW = 0x4
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_TOPK = 32
 MOE_MAX_RANKS = 1024

@@ -381,6 +381,7 @@ static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void
     a.tab_ctas = h->cfg.num_ranks;
   }
   a.P = h->cfg.num_ranks;
+  a.status = h->status;
   if (fixed) {
     a.src_pre = h->src_pre;
     a.slot_Tr = h->cfg.tokens_per_rank;

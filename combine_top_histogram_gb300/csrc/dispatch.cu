@@ -69,10 +69,12 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
     const int t = (int)(g - (long long)s * p.Tr);
     const int b = s * p.cps + t / p.tpc;
     const int pos = __ldg(p.hist + (long long)e * p.nchunks + b) + code_rank(code);
-    if (p.cap <= 0 || pos < p.cap) {
-      r = p.slot_Tr > 0
-              ? (e * p.P + s) * p.slot_Tr + (pos - __ldg(p.src_pre + (long long)s * p.E + e))
-              : __ldg(p.expert_offset + e) + pos;
+    // fixed slots: q is the rank among source s's assignments to e; a region
+    // has slot_Tr rows, enough unless an id repeats within a token
+    const int q = p.slot_Tr > 0 ? pos - __ldg(p.src_pre + (long long)s * p.E + e) : 0;
+    if (p.slot_Tr > 0 && q >= p.slot_Tr) atomicOr(p.status, MOE_STATUS_SLOT_OVERFLOW);
+    if ((p.cap <= 0 || pos < p.cap) && q < max(p.slot_Tr, 1)) {
+      r = p.slot_Tr > 0 ? (e * p.P + s) * p.slot_Tr + q : __ldg(p.expert_offset + e) + pos;
       p.m_local_expert[r] = e % p.L;
       p.m_src_rank[r] = s;
       p.m_src_token[r] = t;

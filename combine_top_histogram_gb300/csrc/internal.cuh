@@ -111,6 +111,7 @@ struct DispatchArgs {
   // assignments to e; src_pre gives the prefix at s's first chunk.
   const int32_t* src_pre;
   int slot_Tr, P;
+  uint32_t* status;       // MOE_STATUS_SLOT_OVERFLOW (fixed slots)
 };
 
 // Persistent single-launch route/layout/dispatch (fused.cu).

@@ -84,6 +84,9 @@ extern "C" {
 /* ---- device status bits (sticky until moe_read_status clears them) ------ */
 #define MOE_STATUS_BAD_EXPERT_ID 0x1u  /* an id outside [-1, E): slot treated as masked */
 #define MOE_STATUS_TIMEOUT 0x2u        /* a bounded device wait gave up */
+#define MOE_STATUS_SLOT_OVERFLOW 0x4u  /* fixed slots: more than T_r assignments of one
+                                          source to one expert (an id repeated within a
+                                          token); the excess is not written, inv = -1 */
 
 /* Problem description. Passed by pointer; copied into the handle. */
 typedef struct {
@@ -227,7 +230,10 @@ int moe_dispatch(moe_handle_t h, const void *x, const float *w, void *recv_x,
  * its rank among source s's assignments to e in (t, j) order. No row depends
  * on another source's counts, so no scan across sources is needed, at the
  * price of E*T rows of storage; region (e, s) holds src_expert_count[s][e]
- * filled rows, the rest untouched. Needs a preceding layout call on a handle
+ * filled rows, the rest untouched. A region holds T_r rows, enough when a
+ * token's k ids are distinct; an assignment beyond them (an id repeated
+ * within a token) is not written, gets inv = -1 and sets
+ * MOE_STATUS_SLOT_OVERFLOW. Needs a preceding layout call on a handle
  * without capacity (MOE_ERR_UNSUPPORTED otherwise, or when the rows exceed
  * int32). slot_x: moe_fixed_slot_rows(cfg) rows of H elements (bf16, or e4m3
  * with fp32 slot_scale [rows, H/128]); meta arrays of that many rows. Same

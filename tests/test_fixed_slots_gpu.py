@@ -104,3 +104,41 @@ def test_fixed_slots_refuse_a_capacity(gpu):
     with pytest.raises(B.MoeError) as ei:
         B.moe_dispatch_fixed_slots(layer.handle, x, layer.w, one, one, meta)
     assert ei.value.code == -2
+
+
+def test_fixed_slots_overflow_with_repeated_ids(gpu):
+    """A region holds T_r rows: enough for distinct ids per token, not when an
+    id repeats within a token. The excess of a (source, expert) pair is not
+    written (inv = -1) and the status reports it; every other assignment lands
+    at its slot row with the oracle's payload."""
+    import torch
+    from combine_top_histogram_gb300 import MoeLayer
+    from combine_top_histogram_gb300 import binding as B
+    P, Tr, E, k, H = 2, 5, 4, 3, 128
+    wl = W.Workload("fs_overflow", P, Tr, E, k, H, W.MOE_BF16, "uniform", "identity")
+    rng = np.random.default_rng(5)
+    ids = rng.integers(0, E, (wl.T, k)).astype(np.int32)
+    ids[:Tr] = 1  # source 0: every slot of every token picks expert 1 (15 > T_r = 5)
+    w = rng.random((wl.T, k)).astype(np.float32)
+    x = W.draw_hidden(rng, wl.T, H)
+    inp = W.Inputs(wl, x, None, ids, w, None)
+    o = run_oracle(wl, inp)
+    want, inv_c = expected_rows(wl, o)
+    q = np.where(want >= 0, want % Tr, 0)
+    region_q = inv_c - o["layout"]["recv_offset"].reshape(P, E)[np.arange(wl.Na) // (Tr * k), ids.reshape(-1)]
+    over = (inv_c >= 0) & (region_q >= Tr)
+    assert over.sum() >= 10  # source 0: 15 assignments to expert 1, 5 fit
+    want = np.where(over, -1, want)
+    layer = MoeLayer(P, Tr, E, k, H)
+    dev = torch.device("cuda")
+    xt = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    layer.layout(torch.from_numpy(ids).to(dev))
+    layer.dispatch_fixed_slots(xt, torch.from_numpy(w).to(dev))
+    torch.cuda.synchronize()
+    assert layer.status() & B.MOE_STATUS_SLOT_OVERFLOW
+    got = layer.layout_view()["inv"].cpu().numpy().astype(np.int64)
+    assert np.array_equal(got, want)
+    ok = want >= 0
+    sel = torch.from_numpy(want[ok]).to(dev)
+    assert np.array_equal(to_np_bits(layer.slots["x"].index_select(0, sel)), o["recv_x"][inv_c[ok]])
+    assert np.all(q[ok] < Tr)
