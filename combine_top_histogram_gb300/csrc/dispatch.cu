@@ -54,14 +54,30 @@ __global__ void __launch_bounds__(kDispatchThreads) k_tables(const TablesArgs t)
   source_tables(t, blockIdx.x, tab_s);
 }
 
+// The assignment code and weight of slot j = threadIdx.x of token g. The
+// codes come from the layout kernel, which is at least two launches before
+// any dispatch (the scan sits between them), so under the launch rule above
+// they are complete when the dispatch starts; the weights are an input, like
+// x. Both may therefore be loaded before the dispatch's wait.
+struct SlotIn {
+  int code;
+  float w;
+};
+__device__ __forceinline__ SlotIn load_slot(const DispatchArgs& p, long long g) {
+  const int j = threadIdx.x;
+  if (j >= p.k) return SlotIn{-1, 0.0f};
+  const long long a = g * p.k + j;
+  return SlotIn{__ldg(p.acode + a), __ldg(p.w + a)};
+}
+
 // Resolves the k receive rows of token g into rows_s, writes inv and the row
-// metadata. Threads 0..k-1 each take one slot.
+// metadata. Threads 0..k-1 each take one slot (in: load_slot of the token).
 __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g, int* rows_s,
-                                             int* owner_s = nullptr) {
+                                             SlotIn in, int* owner_s = nullptr) {
   const int j = threadIdx.x;
   if (j >= p.k) return;
   const long long a = g * p.k + j;
-  const int code = __ldg(p.acode + a);
+  const int code = in.code;
   int r = -1;
   if (code >= 0) {
     const int e = code_expert(code);
@@ -79,7 +95,7 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
       p.m_src_rank[r] = s;
       p.m_src_token[r] = t;
       p.m_slot[r] = j;
-      p.m_weight[r] = __ldg(p.w + a);
+      p.m_weight[r] = in.w;
     }
   }
   p.inv[a] = r;
@@ -107,6 +123,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
+    const SlotIn si = load_slot(p, g);
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -122,7 +139,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
           pdl_trigger();
           waited = true;
         }
-        resolve_rows(p, g, rows_s);
+        resolve_rows(p, g, rows_s, si);
         __syncthreads();
       }
       for (int j = 0; j < p.k; ++j) {
@@ -159,6 +176,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
+    const SlotIn si = load_slot(p, g);
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -175,7 +193,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
           pdl_trigger();
           waited = true;
         }
-        resolve_rows(p, g, rows_s);
+        resolve_rows(p, g, rows_s, si);
         __syncthreads();
       }
 #pragma unroll
@@ -227,6 +245,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
+    const SlotIn si = load_slot(p, g);
     const uint16_t* src = p.x + g * p.H;
     for (int c0 = 0; c0 < nch; c0 += CPT * kDispatchThreads) {
       uint4 va[CPT], vb[CPT];
@@ -246,7 +265,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
           pdl_trigger();
           waited = true;
         }
-        resolve_rows(p, g, rows_s);
+        resolve_rows(p, g, rows_s, si);
         __syncthreads();
       }
 #pragma unroll
@@ -329,7 +348,7 @@ __global__ void __launch_bounds__(kDispatchThreads) k_allgather_filter(const All
   pdl_wait();
   pdl_trigger();
   for (long long g = blockIdx.x; g < p.T; g += gridDim.x) {
-    resolve_rows(p, g, rows_s, owner_s);
+    resolve_rows(p, g, rows_s, load_slot(p, g), owner_s);
     __syncthreads();
     for (int j = 0; j < p.k; ++j) {
       const int r = rows_s[j];

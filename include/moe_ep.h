@@ -47,10 +47,11 @@
  *   - Kernels are launched with programmatic dependent launch: each waits for
  *     the previous grid on the stream before reading what that grid may have
  *     written, and lets its successor launch right after that wait.
- *     moe_dispatch starts loading x before its wait, so x must not be written
- *     by the immediately preceding kernel on the stream if that kernel lets
- *     its dependents launch before it finishes (kernels launched without
- *     programmatic dependent launch, and this library's own kernels, are fine).
+ *     The dispatch entry points start loading x and w before their wait, so
+ *     x and w must not be written by the immediately preceding kernel on the
+ *     stream if that kernel lets its dependents launch before it finishes
+ *     (kernels launched without programmatic dependent launch, and this
+ *     library's own kernels, are fine).
  */
 #ifndef MOE_EP_H
 #define MOE_EP_H
