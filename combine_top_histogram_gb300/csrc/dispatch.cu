@@ -14,12 +14,13 @@
 // One GPU: the P virtual ranks' receive segments are ranges of one receive
 // buffer, so "sending" an assignment is storing its row at its receive row.
 // Each CTA takes one token at a time: reads the bf16 row from HBM once into
-// registers (16-byte loads, coalesced), quantises it once if FP8, and stores
-// it to each of the token's k receive rows (16- or 8-byte stores, coalesced).
-// The receive row of slot j is
+// registers (16-byte loads; 32-byte loads for FP8 when x allows), quantises it
+// once if FP8, and stores it to each of the token's k receive rows (coalesced
+// 16- or 8-byte stores). The receive row of slot j is
 //     r = expert_offset[e] + chunk_base[chunk][e] + chunk-local rank
 // (the stable (expert, source, token, slot) order) and is kept iff its
-// in-expert position is below the capacity.
+// in-expert position is below the capacity. The fixed-slot comparator instead
+// uses (e*P + s)*T_r + (rank among source s's assignments to e).
 //
 // Nothing in the copy needs the per-source tables (cnt, kept counts, receive
 // offsets per source, C and the send offsets), so when the layout deferred
