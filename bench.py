@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -161,14 +162,18 @@ def hbm_peak():
 
 
 def source_sha(kernel: str) -> str:
-    """Fingerprint of a kernel's source: its .cu file and every header of the
-    CUDA sources (a header change may change any kernel)."""
+    """Fingerprint of a kernel's code: its .cu file and every header of the
+    CUDA sources (a header change may change any kernel), with comments and
+    whitespace removed, so that only a change of code voids a measurement."""
     csrc = os.path.join(ROOT, "combine_top_histogram_gb300", "csrc")
     files = [KERNEL_SOURCES[kernel]] + sorted(f for f in os.listdir(csrc) if f.endswith(".cuh"))
     h = hashlib.sha256()
     for name in files:
         with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+            text = f.read()
+        text = re.sub(rb"/\*.*?\*/", b" ", text, flags=re.S)
+        text = re.sub(rb"//[^\n]*", b" ", text)
+        h.update(re.sub(rb"\s+", b" ", text).strip())
     return h.hexdigest()[:16]
 
 
