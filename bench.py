@@ -162,18 +162,28 @@ def hbm_peak():
 
 
 def source_sha(kernel: str) -> str:
-    """Fingerprint of a kernel's code: its .cu file and every header of the
-    CUDA sources (a header change may change any kernel), with comments and
-    whitespace removed, so that only a change of code voids a measurement."""
-    csrc = os.path.join(ROOT, "combine_top_histogram_gb300", "csrc")
-    files = [KERNEL_SOURCES[kernel]] + sorted(f for f in os.listdir(csrc) if f.endswith(".cuh"))
-    h = hashlib.sha256()
-    for name in files:
-        with open(os.path.join(csrc, name), "rb") as f:
+    """Fingerprint of a kernel's code: its .cu file and the headers it
+    includes (transitively, from csrc/ and include/), with comments and
+    whitespace removed, so that only a change of that code voids a
+    measurement."""
+    dirs = [os.path.join(ROOT, "combine_top_histogram_gb300", "csrc"), os.path.join(ROOT, "include")]
+    seen, todo, parts = set(), [KERNEL_SOURCES[kernel]], []
+    while todo:
+        name = todo.pop(0)
+        path = next((os.path.join(d, name) for d in dirs if os.path.exists(os.path.join(d, name))),
+                    None)
+        if name in seen or path is None:
+            continue
+        seen.add(name)
+        with open(path, "rb") as f:
             text = f.read()
         text = re.sub(rb"/\*.*?\*/", b" ", text, flags=re.S)
         text = re.sub(rb"//[^\n]*", b" ", text)
-        h.update(re.sub(rb"\s+", b" ", text).strip())
+        parts.append((name, re.sub(rb"\s+", b" ", text).strip()))
+        todo += [m.decode() for m in re.findall(rb'#include "([^"]+)"', text)]
+    h = hashlib.sha256()
+    for name, code in sorted(parts):
+        h.update(name.encode() + b"\0" + code)
     return h.hexdigest()[:16]
 
 
