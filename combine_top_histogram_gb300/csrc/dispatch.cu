@@ -291,6 +291,84 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
   }
 }
 
+// k_dispatch_fp8w for CTAs that take several tokens: while a token is
+// quantised and stored, each thread copies its own 32-byte chunks of the
+// CTA's next token row into the other half of a two-row shared buffer
+// (cp.async), so the row loads of consecutive tokens overlap the stores
+// instead of waiting behind them. A thread reads back only the bytes it
+// copied, so the staging needs no barrier: cp.async.wait_group orders them.
+// Dynamic shared memory: 2 rows of H bf16 values (and E + 32 ints for the
+// tables CTAs, if larger).
+template <int CPT>
+__global__ void __launch_bounds__(kDispatchThreads, 7) k_dispatch_fp8s(const DispatchArgs p) {
+  extern __shared__ __align__(16) uint16_t xs[];  // [2][H]
+  __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  const int nch = p.H >> 4;
+  const int nblk = p.H >> 7;
+  const int tid = threadIdx.x;
+  if ((int)blockIdx.x < p.tab_ctas) {
+    tables_cta(p);
+    return;
+  }
+  const long long nb = gridDim.x - p.tab_ctas;
+  auto stage = [&](long long tok, int buf) {
+    if (tok < p.T) {
+      const uint16_t* src = p.x + tok * p.H;
+      uint16_t* dst = xs + buf * p.H;
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = i * kDispatchThreads + tid;
+        if (c < nch) {
+          cp_async16(dst + 16 * c, src + 16 * c);
+          cp_async16(dst + 16 * c + 8, src + 16 * c + 8);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  long long g = p.g0 + blockIdx.x - p.tab_ctas;
+  stage(g, 0);
+  bool waited = false;
+  int par = 0;
+  for (; g < p.T; g += nb, par ^= 1) {
+    const SlotIn si = load_slot(p, g);
+    stage(g + nb, par ^ 1);
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    int* rows_s = rows_buf[par];
+    resolve_rows(p, g, rows_s, si);
+    __syncthreads();
+    cp_async_wait_prev();  // this token's chunks (this thread's own copies) have landed
+    const uint16_t* row = xs + par * p.H;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+      const int c = i * kDispatchThreads + tid;
+      uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
+      if (c < nch) {
+        va = *reinterpret_cast<const uint4*>(row + 16 * c);
+        vb = *reinterpret_cast<const uint4*>(row + 16 * c + 8);
+      }
+      float m = fmaxf(amax8(va), amax8(vb));
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const float sc = __fdiv_rn(m, 448.0f);
+      const uint4 code = quant16(va, vb, sc, m);
+      if (c < nch) {
+        for (int j = 0; j < p.k; ++j) {
+          const int r = rows_s[j];
+          if (r < 0) continue;
+          reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.recv) + (long long)r * p.H)[c] = code;
+          if ((tid & 7) == 0) p.recv_scale[(long long)r * nblk + (c >> 3)] = sc;
+        }
+      }
+    }
+  }
+  cp_async_wait_all();  // no copy outlives the CTA
+}
+
 // AllGather comparator, stage 1: every token row (quantised once for FP8) is
 // written to all P ranks' gathered copies, rows d*T + g.
 template <bool FP8, int VPT>
@@ -402,6 +480,15 @@ cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaSt
   const int nvec = a.H >> 3;
   if (fp8 && (reinterpret_cast<uintptr_t>(a.x) & 31) == 0) {
     const int nch = a.H >> 4;
+    // at least 16 tokens per CTA and two rows fit in shared memory: stage rows
+    // ahead (with fewer tokens per CTA the lost CTA per SM costs more)
+    const size_t stage_smem = (size_t)2 * a.H * sizeof(uint16_t);
+    if (a.T - a.g0 >= 16 * blocks && nch <= 4 * kDispatchThreads && stage_smem <= 48 * 1024) {
+      const size_t sm = stage_smem > smem ? stage_smem : smem;
+      if (nch <= 128) return launch_pdl(k_dispatch_fp8s<1>, grid, block, sm, st, a);
+      else if (nch <= 256) return launch_pdl(k_dispatch_fp8s<2>, grid, block, sm, st, a);
+      else return launch_pdl(k_dispatch_fp8s<4>, grid, block, sm, st, a);
+    }
     if (nch <= 128) return launch_pdl(k_dispatch_fp8w<1>, grid, block, smem, st, a);
     else if (nch <= 256) return launch_pdl(k_dispatch_fp8w<2>, grid, block, smem, st, a);
     else return launch_pdl(k_dispatch_fp8w<4>, grid, block, smem, st, a);

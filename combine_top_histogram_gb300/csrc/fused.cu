@@ -68,14 +68,6 @@ __device__ bool grid_barrier(unsigned* c, long long limit, uint32_t* status) {
   return s_ok != 0;
 }
 
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Returns false if a grid barrier timed out.
 template <bool ROUTE, bool FP8, int EPL>
 __device__ __forceinline__ bool fused_body(const FusedArgs& f, int* smem) {

@@ -81,6 +81,23 @@ __device__ __forceinline__ void ld_stream32(const void* p, uint4& a, uint4& b) {
                : "l"(p));
 }
 
+// Asynchronous 16-byte global -> shared copies (cp.async, completion tracked
+// per thread in commit groups; the waits are hardware waits, not spins).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until at most one of this thread's committed groups is still pending.
+__device__ __forceinline__ void cp_async_wait_prev() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Two fp32 lanes in one 64-bit register (first value in the low half) and the
 // packed round-to-nearest multiply and fused multiply-add, each lane rounded
 // exactly as the scalar operation.

@@ -161,6 +161,15 @@ def test_fp8_capacity_parity(gpu, cap):
     _check(wl, inp)
 
 
+def test_fp8_dispatch_many_tokens_per_cta(gpu):
+    """More than 16 tokens per dispatch CTA (T = 40000 over at most 16 CTAs
+    per SM): the FP8 dispatch stages each CTA's next row in shared memory
+    while storing the current one. Every element against the oracle."""
+    wl = W.UNIFORM_FP8.scaled("fp8_staged", Tr=5000, H=256)
+    inp = W.make_inputs(wl)
+    compare(wl, run_gpu(wl, inp), run_oracle(wl, inp), routed=False)
+
+
 @pytest.mark.parametrize("name", ["uniform_fp8", "prefill_cap"])
 def test_fp8_dispatch_with_x_only_16_byte_aligned(gpu, name):
     """x 16- but not 32-byte aligned: the FP8 dispatch takes its 16-byte-load
