@@ -87,7 +87,7 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
     return o;
   };
   p.off_ctrl = take(64);
-  p.off_acc = take((size_t)2 * E * 4);
+  p.off_acc = take((size_t)E * 4);
   p.off_totals = take(4 * sizeof(int32_t));
   p.off_n_raw = take((size_t)E * 4);
   p.off_n_kept = take((size_t)E * 4);
@@ -145,8 +145,7 @@ moe::LayoutArgs layout_args(moe_handle_t h, bool route) {
   a.cap = h->cfg.expert_capacity;
   a.Na = h->Na;
   a.defer_tables = 1;
-  a.acc_add = h->acc + (h->acc_gen & 1ull) * a.E;
-  a.acc_zero = h->acc + ((h->acc_gen + 1ull) & 1ull) * a.E;
+  a.acc_add = h->acc;
   return a;
 }
 
@@ -263,7 +262,7 @@ int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
   h->wait_limit = 1ll << 22;  // ~0.3 s of 64 ns polls
   h->acc = reinterpret_cast<int32_t*>(ws + p.off_acc);
   if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess ||
-      cudaMemset(ws + p.off_acc, 0, (size_t)2 * cfg->num_experts * 4) != cudaSuccess) {
+      cudaMemset(ws + p.off_acc, 0, (size_t)cfg->num_experts * 4) != cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
   }
@@ -286,7 +285,7 @@ static int run_layout(moe_handle_t h, bool route, const int32_t* ids_in, const f
                       int32_t* ids_out, float* w_out, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (h->acc_dirty) {  // a failed launch may have left partial totals
-    if (cudaMemsetAsync(h->acc, 0, (size_t)2 * h->cfg.num_experts * 4, st) != cudaSuccess)
+    if (cudaMemsetAsync(h->acc, 0, (size_t)h->cfg.num_experts * 4, st) != cudaSuccess)
       return MOE_ERR_CUDA;
     h->acc_dirty = 0;
   }
@@ -300,7 +299,6 @@ static int run_layout(moe_handle_t h, bool route, const int32_t* ids_in, const f
     h->acc_dirty = 1;
     return rc;
   }
-  h->acc_gen += 1;
   h->cur_tpc = a.tpc;
   h->cur_cps = a.cps;
   h->layout_gen += 1;
@@ -570,7 +568,6 @@ int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids,
   f.lay = layout_args(h, route);
   f.lay.defer_tables = 0;  // the persistent kernel builds every table itself
   f.lay.acc_add = nullptr;
-  f.lay.acc_zero = nullptr;
   f.lay.ids_in = ids;
   f.lay.logits = logits;
   f.lay.ids_out = ids;

@@ -58,12 +58,12 @@ struct LayoutArgs {
   // source_tables (dispatch CTAs or k_tables). 0: it writes every table.
   int defer_tables;
   // Per-expert totals accumulated by the layout kernel (one integer add per
-  // chunk and expert), or null. With them every scan CTA derives the expert
-  // offsets itself, so the scan needs no arrival counter and no last CTA
-  // (requires defer_tables). acc_zero is the other of two alternating
-  // buffers: the scan clears it for the next layout.
+  // chunk and expert), or null. With them one scan CTA derives the expert
+  // offsets while the others scan columns, so the scan needs no arrival
+  // counter and no last CTA (requires defer_tables). That CTA is the only
+  // reader and clears the totals after reading them, ready for the next
+  // layout: no host-side state, so a captured graph replays correctly.
   int32_t* acc_add;
-  int32_t* acc_zero;
 };
 
 // Per-source tables of the layout, one source rank s per CTA (source_tables):
@@ -241,8 +241,7 @@ struct moe_handle {
       *recv_offset, *rank_base, *hist, *src_pre, *acode, *inv, *send_pos, *src_base;
   unsigned long long layout_gen, dispatch_gen;
   int tables_pending;       // per-source tables of the last layout not yet built
-  int32_t* acc;             // [2][E] per-expert totals, alternating per layout
-  unsigned long long acc_gen;
+  int32_t* acc;             // [E] per-expert totals (zero between layouts)
   int acc_dirty;            // a failed layout launch may have left partial sums
   int fixed_rows;           // the last dispatch wrote fixed per-(source, expert) slots
   long long wait_limit;     // bounded device waits (persistent path)

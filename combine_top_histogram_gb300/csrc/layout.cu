@@ -61,9 +61,9 @@ namespace {
 //
 // With per-expert totals accumulated by the layout kernel (p.acc_add), one
 // extra CTA (the last) turns them into the expert offsets, rank bases and
-// totals and clears the other accumulator for the next layout, while the
-// other CTAs scan columns: no CTA waits for another. Without them, the last
-// CTA to arrive (threadfence + arrival counter) builds the tables.
+// totals and clears them for the next layout, while the other CTAs scan
+// columns: no CTA waits for another. Without them, the last CTA to arrive
+// (threadfence + arrival counter) builds the tables.
 constexpr int kScanRun = 8;
 
 __device__ void offsets_from_totals(const LayoutArgs& p, int* smem) {
@@ -76,11 +76,11 @@ __device__ void offsets_from_totals(const LayoutArgs& p, int* smem) {
   int dr = 0, rw = 0;
   for (int e = tid; e < E; e += NT) {
     const int raw = __ldcg(p.acc_add + e);
+    p.acc_add[e] = 0;  // this CTA is the totals' only reader
     const int kept = (p.cap > 0 && raw > p.cap) ? p.cap : raw;
     sk[e] = kept;
     rw += raw;
     dr += raw - kept;
-    p.acc_zero[e] = 0;
   }
   if (dr) atomicAdd(&red[0], dr);
   if (rw) atomicAdd(&red[1], rw);

@@ -1,8 +1,8 @@
 """One handle through every dispatch mode in turn: separate, persistent,
 fixed slots, two-stage, AllGather, pipelined, separate again. Each layer has
 its own routing (a new seed) and must match the oracle exactly, so the
-handle's state carried between calls (the two alternating per-expert total
-buffers, the per-source tables built by whichever dispatch comes first, the
+handle's state carried between calls (the per-expert totals cleared by each
+scan, the per-source tables built by whichever dispatch comes first, the
 slot-row flag of the expert stand-in) is exercised across every transition."""
 import numpy as np
 import pytest
