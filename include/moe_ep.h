@@ -52,6 +52,10 @@
  *     stream if that kernel lets its dependents launch before it finishes
  *     (kernels launched without programmatic dependent launch, and this
  *     library's own kernels, are fine).
+ *   - Every call that launches work is asynchronous and can be captured in a
+ *     CUDA graph. Capture a layout call together with the dispatch that
+ *     follows it: the layout records on the host that the per-source tables
+ *     are pending, and that dispatch's launch builds them.
  */
 #ifndef MOE_EP_H
 #define MOE_EP_H
