@@ -8,8 +8,6 @@ checks; every step runs in the library's kernels.
 """
 from __future__ import annotations
 
-from typing import Optional
-
 from . import binding as B
 
 

@@ -5,8 +5,6 @@ import ctypes
 import os
 import re
 
-import pytest
-
 from combine_top_histogram_gb300 import binding as B
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
