@@ -48,3 +48,60 @@ def test_one_handle_through_every_mode(gpu, base):
                     allgather=mode == "allgather", pipelined=4 if mode == "pipelined" else 0)
         compare(wl, g, o, routed=routed)
         assert g["status"] == 0, (i, mode)
+
+
+def _inputs_to_device(inp, dev):
+    import torch
+    x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    z = torch.from_numpy(inp.logits).to(dev) if inp.logits is not None else None
+    ids = torch.from_numpy(inp.ids).to(dev) if inp.ids is not None else None
+    w = torch.from_numpy(inp.w).to(dev) if inp.w is not None else None
+    c = torch.from_numpy(inp.expert_scale).to(dev) if inp.expert_scale is not None else None
+    return x, z, ids, w, c
+
+
+def _check_layer(layer, wl, inp):
+    o = run_oracle(wl, inp)
+    view = layer.layout_view()
+    assert np.array_equal(view["inv"].cpu().numpy(), o["layout"]["inv"].reshape(-1))
+    assert bf16_ulp_diff(to_np_bits(layer.out), o["out"]).max() <= 1
+    assert layer.status() == 0
+
+
+def test_two_handles_interleaved_and_on_two_streams(gpu):
+    """Two handles share no state: their calls interleaved on one stream, then
+    two whole layers on two concurrent streams, each exact."""
+    import torch
+    from combine_top_histogram_gb300 import MoeLayer
+    dev = torch.device("cuda")
+    wa = W.DECODE.scaled("pair_a", Tr=37)
+    wb = W.UNIFORM_FP8.scaled("pair_b", Tr=300, H=1024)
+    la = MoeLayer(wa.P, wa.Tr, wa.E, wa.k, wa.H, wa.dispatch_dtype, wa.cap)
+    lb = MoeLayer(wb.P, wb.Tr, wb.E, wb.k, wb.H, wb.dispatch_dtype, wb.cap)
+    ia, ib = W.make_inputs(wa, seed=7), W.make_inputs(wb, seed=8)
+    xa, za, _, _, ca = _inputs_to_device(ia, dev)
+    xb, _, idsb, wbt, cb = _inputs_to_device(ib, dev)
+    # interleaved on the current stream
+    la.route_layout(za)
+    lb.layout(idsb)
+    la.dispatch(xa, la.w)
+    lb.dispatch(xb, wbt)
+    lb.expert(cb)
+    la.expert(ca)
+    la.combine(la.w)
+    lb.combine(wbt)
+    torch.cuda.synchronize()
+    _check_layer(la, wa, ia)
+    _check_layer(lb, wb, ib)
+    # concurrently on two streams, new routings
+    ia, ib = W.make_inputs(wa, seed=9), W.make_inputs(wb, seed=10)
+    xa, za, _, _, ca = _inputs_to_device(ia, dev)
+    xb, _, idsb, wbt, cb = _inputs_to_device(ib, dev)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    la.forward(xa, logits=za, expert_scale=ca, stream=sa)
+    lb.forward(xb, ids=idsb, w=wbt, expert_scale=cb, stream=sb)
+    torch.cuda.synchronize()
+    _check_layer(la, wa, ia)
+    _check_layer(lb, wb, ib)
