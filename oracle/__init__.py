@@ -29,6 +29,7 @@ import ctypes
 import os
 import subprocess
 import threading
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -105,6 +106,36 @@ def _c(a, dtype):
 
 
 # --------------------------------------------------------------------------
+# token-range shards (marshalling only: the C functions run unchanged)
+# --------------------------------------------------------------------------
+def _ranges(n: int, threads: int):
+    """[a, b) token ranges of about n / threads tokens each."""
+    threads = max(1, min(int(threads), n))
+    b = [n * i // threads for i in range(threads + 1)]
+    return [(b[i], b[i + 1]) for i in range(threads) if b[i + 1] > b[i]]
+
+
+def _run(jobs):
+    """Runs the jobs (calls into the C library, which release the GIL) on one
+    thread each; a single job runs inline."""
+    if len(jobs) <= 1:
+        for j in jobs:
+            j()
+        return
+    with ThreadPoolExecutor(len(jobs)) as ex:
+        for f in [ex.submit(j) for j in jobs]:
+            f.result()
+
+
+def _shard_inv(inv: np.ndarray, k: int, a: int, b: int) -> np.ndarray:
+    """inv with every assignment outside tokens [a, b) marked -1, so that an
+    unchanged dispatch call writes exactly the rows of those tokens."""
+    out = np.full_like(inv, -1)
+    out[a * k:b * k] = inv[a * k:b * k]
+    return out
+
+
+# --------------------------------------------------------------------------
 # number formats
 # --------------------------------------------------------------------------
 def bf16_from_f32(v: float) -> int:
@@ -126,14 +157,17 @@ def e4m3_from_f32(v: float) -> int:
 # --------------------------------------------------------------------------
 # path steps
 # --------------------------------------------------------------------------
-def route_topk(logits: np.ndarray, k: int):
+def route_topk(logits: np.ndarray, k: int, threads: int = 1):
     """Top-k ids (descending logit, ties to the lower expert) and the softmax of
-    the chosen logits (double, rounded to fp32)."""
+    the chosen logits (double, rounded to fp32). threads > 1 runs the same C
+    function on token ranges concurrently (tokens are independent)."""
     z = _c(logits, np.float32)
     T, E = z.shape
     ids = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float32)
-    _load().oref_route_topk(T, E, k, z, ids, w)
+    lib = _load()
+    _run([lambda a=a, b=b: lib.oref_route_topk(b - a, E, k, z[a:b], ids[a:b], w[a:b])
+          for a, b in _ranges(T, threads)])
     return ids, w
 
 
@@ -164,29 +198,48 @@ def _meta(rows):
 
 
 def dispatch_bf16(P, Tr, E, k, x_bits: np.ndarray, w: np.ndarray, ids: np.ndarray,
-                  inv: np.ndarray, rows: int):
-    """Receive rows [rows, H] (bf16 bits) and metadata, from x bits [T, H]."""
+                  inv: np.ndarray, rows: int, threads: int = 1):
+    """Receive rows [rows, H] (bf16 bits) and metadata, from x bits [T, H].
+    threads > 1: each thread runs the same C function with the assignments of
+    its token range only (the others marked -1); the rows they write are
+    disjoint."""
     x_bits = _c(x_bits, np.uint16)
-    H = x_bits.shape[1]
+    T, H = x_bits.shape
     recv = np.zeros((rows, H), np.uint16)
     m = _meta(rows)
-    _load().oref_dispatch_bf16(P, Tr, E, k, H, _c(ids, np.int32).reshape(-1),
-                               _c(inv, np.int32).reshape(-1), x_bits,
-                               _c(w, np.float32).reshape(-1), recv, m["local_expert"],
-                               m["src_rank"], m["src_token"], m["slot"], m["weight"])
+    ids_f, inv_f, w_f = (_c(ids, np.int32).reshape(-1), _c(inv, np.int32).reshape(-1),
+                         _c(w, np.float32).reshape(-1))
+    lib = _load()
+    parts = _ranges(T, threads)
+
+    def job(a, b):
+        inv_s = inv_f if len(parts) == 1 else _shard_inv(inv_f, k, a, b)
+        lib.oref_dispatch_bf16(P, Tr, E, k, H, ids_f, inv_s, x_bits, w_f, recv,
+                               m["local_expert"], m["src_rank"], m["src_token"], m["slot"],
+                               m["weight"])
+    _run([lambda a=a, b=b: job(a, b) for a, b in parts])
     return recv, m
 
 
-def dispatch_fp8(P, Tr, E, k, x_bits, w, ids, inv, rows: int):
+def dispatch_fp8(P, Tr, E, k, x_bits, w, ids, inv, rows: int, threads: int = 1):
+    """FP8 receive rows [rows, H] (e4m3 codes), scales [rows, H/128] and
+    metadata; threads as in dispatch_bf16."""
     x_bits = _c(x_bits, np.uint16)
-    H = x_bits.shape[1]
+    T, H = x_bits.shape
     recv = np.zeros((rows, H), np.uint8)
     sc = np.zeros((rows, H // 128), np.float32)
     m = _meta(rows)
-    _load().oref_dispatch_fp8(P, Tr, E, k, H, _c(ids, np.int32).reshape(-1),
-                              _c(inv, np.int32).reshape(-1), x_bits,
-                              _c(w, np.float32).reshape(-1), recv, sc, m["local_expert"],
-                              m["src_rank"], m["src_token"], m["slot"], m["weight"])
+    ids_f, inv_f, w_f = (_c(ids, np.int32).reshape(-1), _c(inv, np.int32).reshape(-1),
+                         _c(w, np.float32).reshape(-1))
+    lib = _load()
+    parts = _ranges(T, threads)
+
+    def job(a, b):
+        inv_s = inv_f if len(parts) == 1 else _shard_inv(inv_f, k, a, b)
+        lib.oref_dispatch_fp8(P, Tr, E, k, H, ids_f, inv_s, x_bits, w_f, recv, sc,
+                              m["local_expert"], m["src_rank"], m["src_token"], m["slot"],
+                              m["weight"])
+    _run([lambda a=a, b=b: job(a, b) for a, b in parts])
     return recv, sc, m
 
 
@@ -207,20 +260,30 @@ def expert_scale_bf16(E, expert_offset, c, recv_bits):
     return y
 
 
-def expert_dequant_fp8(recv_q, recv_scale):
+def expert_dequant_fp8(recv_q, recv_scale, threads: int = 1):
+    """threads > 1: the same C function on row ranges (rows are independent)."""
     recv_q = _c(recv_q, np.uint8)
     rows, H = recv_q.shape
     y = np.zeros((rows, H), np.uint16)
-    _load().oref_expert_dequant_fp8(rows, H, recv_q, _c(recv_scale, np.float32), y)
+    s = _c(recv_scale, np.float32)
+    lib = _load()
+    _run([lambda a=a, b=b: lib.oref_expert_dequant_fp8(b - a, H, recv_q[a:b], s[a:b], y[a:b])
+          for a, b in _ranges(rows, threads)])
     return y
 
 
-def combine(inv: np.ndarray, w: np.ndarray, y_bits: np.ndarray, T: int, k: int):
+def combine(inv: np.ndarray, w: np.ndarray, y_bits: np.ndarray, T: int, k: int,
+            threads: int = 1):
+    """threads > 1: the same C function on token ranges (each output token
+    reads only its own slots)."""
     y_bits = _c(y_bits, np.uint16)
     H = y_bits.shape[1]
     out = np.empty((T, H), np.uint16)
-    _load().oref_combine(T, k, H, _c(inv, np.int32).reshape(-1),
-                         _c(w, np.float32).reshape(-1), y_bits, out)
+    inv_f, w_f = _c(inv, np.int32).reshape(-1), _c(w, np.float32).reshape(-1)
+    lib = _load()
+    _run([lambda a=a, b=b: lib.oref_combine(b - a, k, H, inv_f[a * k:b * k], w_f[a * k:b * k],
+                                            y_bits, out[a:b])
+          for a, b in _ranges(T, threads)])
     return out
 
 

@@ -277,6 +277,90 @@ def test_dispatch_bf16_rows_are_the_source_rows():
         assert m["local_expert"][r] == ids[g, j] % (E // P) and m["weight"][r] == w[g, j]
 
 
+def test_dispatch_fp8_rows_scales_and_metadata():
+    """The FP8 dispatch's placement, pinned row by row from outside the
+    dispatch: every kept assignment a = (g, j) with row r = inv[a] holds the
+    quantised token row (codes and scales of the separately pinned per-row
+    quantiser) at payload row r and scale row r, and the metadata named by the
+    pages' payload schema (local expert, source rank and token, slot, weight);
+    rows at or beyond the kept count keep their fill. The ids are masked in
+    places and a capacity drops rows, so some tokens have every slot dropped
+    and some only a few."""
+    rng = np.random.default_rng(15)
+    P, Tr, E, k, H = 3, 11, 6, 3, 384  # three 128-channel blocks per row
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(P * Tr)]).astype(np.int32)
+    ids[rng.random(ids.shape) < 0.2] = -1
+    ids[4] = -1  # a token with every slot masked
+    w = rng.random((P * Tr, k)).astype(np.float32)
+    # each token row has its own scale per block, so a row or scale taken from
+    # the wrong token or block cannot match
+    mag = 10.0 ** rng.integers(-3, 3, (P * Tr, H // 128)).repeat(128, axis=1)
+    x = bf16_bits(rng.standard_normal((P * Tr, H)) * mag)
+    x[7, 128:256] = 0  # an all-zero block
+    cap = 4
+    lay = oracle.layout(P, Tr, E, k, ids, cap)
+    inv = lay["inv"].reshape(P * Tr, k)
+    rows = P * Tr * k
+    q, sc, m = oracle.dispatch_fp8(P, Tr, E, k, x, w, ids, lay["inv"], rows)
+    nk = int(lay["totals"][0])
+    assert lay["totals"][1] > 0  # the capacity dropped something
+    full_drop = [g for g in range(P * Tr)
+                 if (ids[g] >= 0).any() and (inv[g] < 0).all()]
+    partial = [g for g in range(P * Tr) if (inv[g] >= 0).any() and (inv[g] < 0).any()
+               and (ids[g] >= 0).all()]
+    assert full_drop and partial  # both kinds of token occur
+    seen = np.zeros(rows, bool)
+    for g in range(P * Tr):
+        want_q, want_s = oracle.quantize_row_fp8(x[g])
+        for j in range(k):
+            r = int(inv[g, j])
+            if r < 0:
+                continue
+            assert not seen[r]
+            seen[r] = True
+            assert np.array_equal(q[r], want_q), (g, j)
+            assert np.array_equal(sc[r].view(np.uint32), want_s.view(np.uint32)), (g, j)
+            assert m["local_expert"][r] == ids[g, j] % (E // P)
+            assert m["src_rank"][r] == g // Tr and m["src_token"][r] == g % Tr
+            assert m["slot"][r] == j and m["weight"][r] == w[g, j]
+    assert seen[:nk].all() and not seen[nk:].any()
+    # untouched fill past the kept rows
+    assert not q[nk:].any() and not sc[nk:].any()
+    for name in ("local_expert", "src_rank", "src_token", "slot"):
+        assert (m[name][nk:] == -7).all()
+    assert np.isnan(m["weight"][nk:]).all()
+
+
+def test_token_range_threads_give_the_same_results():
+    """The oracle's threads option only splits tokens across threads; every
+    output must equal the single-threaded call's."""
+    rng = np.random.default_rng(16)
+    P, Tr, E, k, H = 3, 13, 12, 4, 256
+    z = rng.standard_normal((P * Tr, E)).astype(np.float32)
+    ids1, w1 = oracle.route_topk(z, k)
+    ids4, w4 = oracle.route_topk(z, k, threads=4)
+    assert np.array_equal(ids1, ids4) and np.array_equal(w1.view(np.int32), w4.view(np.int32))
+    x = bf16_bits(rng.standard_normal((P * Tr, H)))
+    lay = oracle.layout(P, Tr, E, k, ids1, 9)
+    rows = P * Tr * k
+    a = oracle.dispatch_fp8(P, Tr, E, k, x, w1, ids1, lay["inv"], rows)
+    b = oracle.dispatch_fp8(P, Tr, E, k, x, w1, ids1, lay["inv"], rows, threads=5)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1].view(np.int32), b[1].view(np.int32))
+    for n in a[2]:
+        assert np.array_equal(a[2][n].view(np.int32), b[2][n].view(np.int32)), n
+    c = oracle.dispatch_bf16(P, Tr, E, k, x, w1, ids1, lay["inv"], rows)
+    d = oracle.dispatch_bf16(P, Tr, E, k, x, w1, ids1, lay["inv"], rows, threads=3)
+    assert np.array_equal(c[0], d[0])
+    for n in c[1]:
+        assert np.array_equal(c[1][n].view(np.int32), d[1][n].view(np.int32)), n
+    y1 = oracle.expert_dequant_fp8(a[0], a[1])
+    y3 = oracle.expert_dequant_fp8(a[0], a[1], threads=3)
+    assert np.array_equal(y1, y3)
+    o1 = oracle.combine(lay["inv"], w1, y1, P * Tr, k)
+    o6 = oracle.combine(lay["inv"], w1, y1, P * Tr, k, threads=6)
+    assert np.array_equal(o1, o6)
+
+
 def test_quantize_fp8_error_bound_and_closed_checks():
     rng = np.random.default_rng(6)
     H = 1024
