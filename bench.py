@@ -10,8 +10,13 @@ L2 flushed (a 320 MB write, then a 320 MB read so that no dirty line of the
 flush is written back inside a timed kernel) before the dispatch phase and
 again before the combine phase of every step, so every phase starts cold.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|...]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill|decode|...]
   python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+The default workload is the largest one that fits one GPU: prefill, 32 virtual
+ranks x 4096 tokens, 256 experts, top-8, H 7168, FP8 dispatch with BF16
+combine, per-expert capacity 5120 (1,048,576 assignments). The value is the
+median over the timed steps.
 
 Under torchrun (N > 1) every rank runs an independent replica (the path has no
 cross-GPU exchange on one GPU per box) and rank 0 prints the max over ranks.
@@ -42,10 +47,12 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="decode")
+    ap.add_argument("--config", default="prefill")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="threads of the multi-threaded oracle baseline (0: all host cores)")
     ap.add_argument("--dispatch", default="separate",
                     choices=["separate", "fused", "two_stage", "allgather", "fixed_slots"],
                     help="separate: layout kernels then the dispatch kernel; fused: one "
@@ -204,17 +211,22 @@ def committed_traffic(kernel: str, workload: str):
 # ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
-def oracle_layer_seconds(wl, budget_s: float, max_layers: int = 50):
+def oracle_layer_seconds(wl, budget_s: float, max_layers: int = 50, threads: int = 1,
+                         elems_target: float = 6.0e7):
     """Times the CPU oracle's route/layout + dispatch + combine (the expert
     stand-in is run untimed) on a bounded sample of the workload: the same
     per-token distribution with fewer tokens per rank when a full layer would
-    take too long. Returns (seconds per full layer, sample description, layers)."""
+    take too long (about elems_target token-row elements, T*k*H). With
+    threads > 1 the route, dispatch and combine run the unchanged oracle
+    functions on token ranges, one thread each; the layout (one global stable
+    sort) stays on one thread. Returns (seconds per full layer, sample
+    description, layers, per-layer times)."""
     import numpy as np
 
     import oracle
     from combine_top_histogram_gb300 import workloads as W
     elems = wl.T * wl.k * wl.H
-    scale = max(1.0, elems / 6.0e7)
+    scale = max(1.0, elems / elems_target)
     tr = max(1, int(wl.Tr / scale))
     sw = wl.scaled(wl.name + "_cpu_sample", Tr=tr)
     if wl.cap:
@@ -226,39 +238,53 @@ def oracle_layer_seconds(wl, budget_s: float, max_layers: int = 50):
     while len(times) < max_layers and (time.perf_counter() - t_start) < budget_s or len(times) < 1:
         t0 = time.perf_counter()
         if inp.logits is not None:
-            ids, w = oracle.route_topk(inp.logits, sw.k)
+            ids, w = oracle.route_topk(inp.logits, sw.k, threads=threads)
         else:
             ids, w = inp.ids, inp.w
         lay = oracle.layout(sw.P, sw.Tr, sw.E, sw.k, ids, sw.cap)
         if fp8:
             recv, sc, _ = oracle.dispatch_fp8(sw.P, sw.Tr, sw.E, sw.k, inp.x, w, ids, lay["inv"],
-                                              sw.rows_max)
+                                              sw.rows_max, threads=threads)
         else:
             recv, _ = oracle.dispatch_bf16(sw.P, sw.Tr, sw.E, sw.k, inp.x, w, ids, lay["inv"],
-                                           sw.rows_max)
+                                           sw.rows_max, threads=threads)
         t1 = time.perf_counter()
         if fp8:
-            y = oracle.expert_dequant_fp8(recv, sc)
+            y = oracle.expert_dequant_fp8(recv, sc, threads=threads)
         else:
             c = inp.expert_scale if inp.expert_scale is not None else np.ones(sw.E, np.float32)
             y = oracle.expert_scale_bf16(sw.E, lay["expert_offset"], c, recv)
         t2 = time.perf_counter()
-        oracle.combine(lay["inv"], w, y, sw.T, sw.k)
+        oracle.combine(lay["inv"], w, y, sw.T, sw.k, threads=threads)
         t3 = time.perf_counter()
         times.append((t1 - t0) + (t3 - t2))
     per_layer = statistics.median(times) * (wl.Tr / tr)
+    how = ("single-threaded C, -O2" if threads <= 1 else
+           f"C, -O2, route/dispatch/combine on {threads} threads over token ranges, "
+           "layout on one thread")
     sample = (f"{len(times)} oracle layers of {sw.T} tokens ({tr} per rank, same config), "
-              f"scaled x{wl.Tr / tr:.2f} to {wl.T} tokens; single-threaded C, -O2")
+              f"median scaled x{wl.Tr / tr:.2f} to {wl.T} tokens; {how}")
     return per_layer, sample, len(times), times
 
 
+def host_threads(args) -> int:
+    return args.cpu_threads if args.cpu_threads > 0 else (os.cpu_count() or 1)
+
+
 def run_reference(args, wl, rank, world):
+    """The reference arm: the CPU oracle as it stands, on all host cores
+    (token-range threads), one bounded sample of the workload per step, sized
+    so that the whole --steps/--warmup run stays within a few minutes."""
     if rank != 0:
         return 0
+    threads = host_threads(args)
+    n = args.warmup + args.steps
+    target = 6.0e7 * threads * min(1.0, 25.0 / max(1, n))
     per_step = []
     desc = None
-    for i in range(args.warmup + args.steps):
-        s, desc, _, _ = oracle_layer_seconds(wl, budget_s=0.0, max_layers=1)
+    for i in range(n):
+        s, desc, _, _ = oracle_layer_seconds(wl, budget_s=0.0, max_layers=1, threads=threads,
+                                             elems_target=target)
         if i >= args.warmup:
             per_step.append(s)
     us = statistics.median(per_step) * 1e6
@@ -268,7 +294,7 @@ def run_reference(args, wl, rank, world):
         "ms_per_step": round(us / 1e3, 4), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.dispatch_dtype == 0 else "fp8_e4m3+bf16",
         "data": "synthetic", "config": {"workload": wl.name},
-        "cpu_baseline": {"value": round(us, 3), "unit": "us/layer", "cores": 1,
+        "cpu_baseline": {"value": round(us, 3), "unit": "us/layer", "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(us, 3), "unit": "us/layer", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -305,7 +331,7 @@ def run_ours(args, wl, rank, world, local):
     # the dirty lines of the write are written back here, outside the timed
     # region, and the next phase starts with a cold, clean L2.
     flush_w = torch.empty(320 << 20, dtype=torch.uint8, device=dev)
-    flush_r = torch.ones(80 << 20, dtype=torch.int32, device=dev)
+    flush_r = torch.ones(80 << 20, dtype=torch.float32, device=dev)
 
     def flush_l2():
         flush_w.zero_()
@@ -382,8 +408,9 @@ def run_ours(args, wl, rank, world, local):
         torch.cuda.synchronize(dev)
     barrier(world)
     step_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs]
-    mean_ms = statistics.fmean(step_ms)
-    mean_ms_all = max_over_ranks(mean_ms, world)
+    med_ms = statistics.median(step_ms)
+    med_ms_all = max_over_ranks(med_ms, world)
+    mean_ms_all = max_over_ranks(statistics.fmean(step_ms), world)
 
     # per-kernel breakdown (events between kernels; diagnostic, same workload)
     devs = new_events(min(args.steps, 50))
@@ -425,7 +452,7 @@ def run_ours(args, wl, rank, world, local):
     for ev in wevs:
         step(ev, flush=False)
     torch.cuda.synchronize(dev)
-    warm_ms = statistics.fmean([e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in wevs])
+    warm_ms = statistics.median([e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in wevs])
 
     # end to end through the public API: pinned host inputs -> device, layer,
     # result -> pinned host, copies inside the timed region
@@ -459,7 +486,7 @@ def run_ours(args, wl, rank, world, local):
     torch.cuda.synchronize(dev)
     for ev in eevs[3:]:
         e2e_ms.append(ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]))
-    e2e_us = max_over_ranks(statistics.fmean(e2e_ms) * 1e3, world)
+    e2e_us = max_over_ranks(statistics.median(e2e_ms) * 1e3, world)
 
     view = layer.layout_view()
     kept = int(view["totals"][0].item())
@@ -502,16 +529,21 @@ def run_ours(args, wl, rank, world, local):
     peak, peak_kind = hbm_peak()
     achieved = bytes_of[dom] / (means[dom] * 1e-3) / 1e9
     traffic = committed_traffic(dom, wl.name) if dom in KERNEL_SOURCES else None
-    cpu = None
+    per_kernel_gbs = {k: round(bytes_of[k] / (v * 1e-3) / 1e9, 1) for k, v in means.items()}
+    cpu = cpu_mt = None
     if rank == 0 and world >= 1 and not args.no_cpu_baseline and world == 1:
         s, desc, n, _ = oracle_layer_seconds(wl, args.cpu_seconds)
         cpu = {"value": round(s * 1e6, 1), "unit": "us/layer", "cores": 1, "kind": "oracle",
                "sample": desc}
-    value_us = mean_ms_all * 1e3
+        nt = host_threads(args)
+        s, desc, n, _ = oracle_layer_seconds(wl, args.cpu_seconds, threads=nt)
+        cpu_mt = {"value": round(s * 1e6, 1), "unit": "us/layer", "cores": nt, "kind": "oracle",
+                  "sample": desc}
+    value_us = med_ms_all * 1e3
     line = {
         "metric": METRIC, "value": round(value_us, 3), "unit": "us/layer",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(mean_ms_all, 5), "higher_is_better": False, "scaling": "weak",
+        "ms_per_step": round(med_ms_all, 5), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None,
         "dtype": "fp8_e4m3+bf16" if layer.fp8 else "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "P": wl.P, "tokens_per_rank": wl.Tr, "E": wl.E,
@@ -524,15 +556,18 @@ def run_ours(args, wl, rank, world, local):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes": bytes_of[dom]},
         "cpu_baseline": cpu,
+        "cpu_baseline_mt": cpu_mt,
         "e2e": {"value": round(e2e_us, 3), "unit": "us/layer", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": (2 if args.dispatch == "fused" else 6 if args.dispatch == "two_stage"
                          else 5 if args.dispatch == "allgather" else 4) * args.steps,
         "clocks": clk.summary(),
         "per_kernel_us": {k: round(v * 1e3, 3) for k, v in means.items()},
-        "assignments_per_s": round(world * wl.Na / (mean_ms_all * 1e-3), 1),
-        "effective_gbs": round((kb.layout + kb.dispatch + kb.combine) / (mean_ms_all * 1e-3) / 1e9, 1),
-        "payload_gbs": round(pay["total"] / (mean_ms_all * 1e-3) / 1e9, 1),
+        "per_kernel_gbs": per_kernel_gbs,
+        "mean_us_per_layer": round(mean_ms_all * 1e3, 3),
+        "assignments_per_s": round(world * wl.Na / (med_ms_all * 1e-3), 1),
+        "effective_gbs": round((kb.layout + kb.dispatch + kb.combine) / (med_ms_all * 1e-3) / 1e9, 1),
+        "payload_gbs": round(pay["total"] / (med_ms_all * 1e-3) / 1e9, 1),
         "warm_us_per_layer": round(warm_ms * 1e3, 3),
         "kept_rows": kept,
         "routing": routing_shape,

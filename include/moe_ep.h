@@ -164,7 +164,11 @@ typedef struct {
     float *weight;         /* w[g, j] */
 } moe_recv_meta_t;
 
-/* Bytes of device workspace a handle for *cfg needs (0 if *cfg is invalid). */
+/* Bytes of device workspace a handle for *cfg needs (0 if *cfg is invalid):
+ * every count, offset, chunk table and per-assignment array of the layout,
+ * sized by the worst case T*k so that no call reads a count back to the host
+ * ([EP] "Memory is not only expert weights": preallocate the EP buffers by
+ * the maximum token count and reuse them across layers). */
 size_t moe_workspace_bytes(const moe_config_t *cfg);
 
 /* Receive rows every recv_* buffer must hold: T*k, or E*c when a capacity c is
@@ -173,14 +177,19 @@ size_t moe_workspace_bytes(const moe_config_t *cfg);
 int64_t moe_recv_rows_max(const moe_config_t *cfg);
 
 /* Creates a handle over d_workspace (device, >= moe_workspace_bytes(cfg)
- * bytes, 256-byte aligned, owned by the caller and not freed by the library).
+ * bytes, 256-byte aligned, owned by the caller and not freed by the library):
+ * the preallocated, reusable EP state of one layer configuration ([EP]
+ * "Memory is not only expert weights"; the combine handle of [EP] "Combine is
+ * not simply sending results back" lives in it: inv, the per-expert counts
+ * and the offsets of the last dispatch).
  * Zeroes the workspace's control words with a synchronous cudaMemset on the
  * current device; call once at set-up, outside stream capture.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 int moe_handle_create(const moe_config_t *cfg, void *d_workspace, size_t bytes,
                       moe_handle_t *out);
 
-/* Frees the host-side handle only. NULL is accepted. */
+/* Housekeeping (no counterpart on the pages): frees the host-side handle
+ * only. NULL is accepted. */
 int moe_handle_destroy(moe_handle_t h);
 
 /* a1 -- router top-k ([PPLX] introduction; [EP] router output [T, k]).
@@ -370,8 +379,9 @@ int moe_expert_standin_tokens(moe_handle_t h, int64_t token_begin, int64_t token
 int moe_combine_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end, const void *y,
                        const float *w, void *out, void *stream);
 
-/* Reads and clears the device status word. Synchronises `stream`: tests and
- * debugging only. *flags receives MOE_STATUS_* bits. */
+/* Housekeeping (no counterpart on the pages): reads and clears the device
+ * status word. Synchronises `stream`: tests and debugging only. *flags
+ * receives MOE_STATUS_* bits. */
 int moe_read_status(moe_handle_t h, uint32_t *flags, void *stream);
 
 /* Human-readable name of a MOE_ERR_* code (static string). */
