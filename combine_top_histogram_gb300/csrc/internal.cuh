@@ -206,6 +206,7 @@ cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long 
 size_t layout_smem_bytes(int E, int tpc, int k, int P);
 size_t scan_smem_bytes(int E, int P);
 cudaError_t layout_prepare(int E, int tpc, int k, int P);
+cudaError_t layout_prepare_all(size_t* layout_dyn_max, size_t* scan_dyn_max);
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st);
 cudaError_t launch_tables(const TablesArgs& t, cudaStream_t st);
 cudaError_t launch_combine(const CombineArgs& a, int num_sms, cudaStream_t st);

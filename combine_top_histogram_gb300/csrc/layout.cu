@@ -257,6 +257,38 @@ cudaError_t layout_prepare(int E, int tpc, int k, int P) {
   return cudaSuccess;
 }
 
+// Raises the dynamic shared-memory limit of every layout kernel variant
+// (given ids, any experts-per-lane) and of the scan kernel to the device's
+// opt-in maximum, once, and reports how much dynamic shared memory each may
+// then take: for callers that set up once and later only launch.
+cudaError_t layout_prepare_all(size_t* layout_dyn_max, size_t* scan_dyn_max) {
+  int dev = 0, optin = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  size_t lay_min = (size_t)optin;
+  for (int epl = 1; epl <= 32; epl <<= 1) {
+    void* fn = layout_kernel_ptr<false>(epl);
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, fn);
+    if (err != cudaSuccess) return err;
+    const int dyn_max = optin - (int)fa.sharedSizeBytes;
+    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
+    if (err != cudaSuccess) return err;
+    if ((size_t)dyn_max < lay_min) lay_min = (size_t)dyn_max;
+  }
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, (void*)k_scan);
+  if (err != cudaSuccess) return err;
+  const int scan_max = optin - (int)fa.sharedSizeBytes;
+  err = cudaFuncSetAttribute((void*)k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, scan_max);
+  if (err != cudaSuccess) return err;
+  *layout_dyn_max = lay_min;
+  *scan_dyn_max = (size_t)scan_max;
+  return cudaSuccess;
+}
+
 cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cudaStream_t st) {
   const size_t smem = layout_smem_bytes(a.E, a.tpc, a.k, a.P);
   const int epl = experts_per_lane(a.E);

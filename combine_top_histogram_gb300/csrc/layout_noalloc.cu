@@ -2,13 +2,15 @@
 // (and the inverse permutation) for callers that cannot allocate device
 // memory, with the library's scratch in a fixed file-scope device array.
 //
-// Who needs this: code that runs where cudaMalloc is off limits -- inside a
-// region being captured into a CUDA graph, inside a host framework that hands
-// out no workspace (some plugin interfaces give only inputs and outputs), or
-// in a process whose allocator is owned by someone else. Such a caller still
-// provides the ids and every output array; the intermediate chunk histograms,
-// per-assignment codes and the arrival counter live in g_noalloc_scratch below
-// instead of a caller workspace.
+// Who needs this: code that may not call cudaMalloc -- a host framework whose
+// plugin interface hands over only inputs and outputs and no workspace, a
+// process whose device memory belongs to another allocator (a framework's
+// caching allocator, a fixed memory budget) that an extra cudaMalloc would
+// overrun or bypass, and code that must not let an allocation or a free
+// synchronise the device. Such a caller still provides the ids and every
+// output array; the intermediate chunk histograms, per-assignment codes and
+// the arrival counter live in g_noalloc_scratch below instead of a caller
+// workspace.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,22 +27,67 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached. Returns nullptr on failure.
-void* scratch_address(int device) {
+// What the entry point needs from a device, looked up once per device context:
+// the scratch array's device address and the dynamic shared memory the layout
+// and scan kernels may take (their limits raised once, here, so that later
+// calls only launch).
+struct DeviceSetup {
+  unsigned long long ctx_id;  // context the entries below belong to
+  void* scratch;
+  size_t layout_dyn_max, scan_dyn_max;
+};
+std::mutex g_mu;
+DeviceSetup g_setup[kMaxDevices] = {};
+
+typedef int (*CtxGetCurrentFn)(void** ctx);
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+
+// Id of the current device context (the driver's cuCtxGetCurrent and
+// cuCtxGetId, reached through the runtime so the library needs no link to the
+// driver library). A device reset ends the context, and the next one has a new
+// id, so nothing cached for an earlier context is used again.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) ==
+            cudaSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) ==
+            cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(f1);
+      get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+    looked_up = true;
+  }
+  if (!get_cur || !get_id) return false;
+  void* ctx = nullptr;
+  if (get_cur(&ctx) != 0 || ctx == nullptr) return false;
+  return get_id(ctx, id) == 0;
+}
+
+// The set-up of the current device, done on the first call in each device
+// context: cudaGetSymbolAddress (which also makes the device's primary context
+// current) and the kernels' shared-memory limits. Returns nullptr on failure.
+const DeviceSetup* device_setup(int device) {
   if (device < 0 || device >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[device] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_scratch_addr[device] = p;
-  }
-  return g_scratch_addr[device];
+  DeviceSetup& d = g_setup[device];
+  unsigned long long id = 0;
+  if (d.scratch != nullptr && current_context_id(&id) && id == d.ctx_id) return &d;
+  DeviceSetup n{};
+  if (cudaGetSymbolAddress(&n.scratch, g_noalloc_scratch) != cudaSuccess) return nullptr;
+  if (moe::layout_prepare_all(&n.layout_dyn_max, &n.scan_dyn_max) != cudaSuccess) return nullptr;
+  if (!current_context_id(&n.ctx_id)) return nullptr;
+  d = n;
+  return &d;
 }
 
 // Receive row of every assignment from its code, the exclusive chunk bases
@@ -66,6 +113,16 @@ __global__ void k_inv_from_codes(const int32_t* __restrict__ acode,
   }
 }
 
+// Tokens per layout chunk of this entry point: whole tokens, about 2048
+// assignments per chunk, never crossing a source rank.
+int chunk_tokens(const moe_config_t* c) {
+  int tpc = 2048 / c->top_k;
+  if (tpc < 1) tpc = 1;
+  if (tpc > moe::kMaxChunkAssign / c->top_k) tpc = moe::kMaxChunkAssign / c->top_k;
+  if (tpc > c->tokens_per_rank) tpc = c->tokens_per_rank;
+  return tpc;
+}
+
 int check_config(const moe_config_t* c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->num_ranks < 1 || c->tokens_per_rank < 1 || c->num_experts < 1 || c->top_k < 1 ||
@@ -74,6 +131,12 @@ int check_config(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->num_experts > MOE_MAX_EXPERTS || c->top_k > MOE_MAX_TOPK ||
       c->num_ranks > MOE_MAX_RANKS)
+    return MOE_ERR_UNSUPPORTED;
+  // The layout kernel keeps per-warp counters and the chunk's ids in shared
+  // memory, and the scan's last CTA every per-(source, expert) prefix.
+  if (moe::layout_smem_bytes(c->num_experts, chunk_tokens(c), c->top_k, c->num_ranks) >
+          moe::kLayoutSmemLimit ||
+      moe::scan_smem_bytes(c->num_experts, c->num_ranks) > moe::kLayoutSmemLimit)
     return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -91,12 +154,7 @@ extern "C" int moe_dispatch_layout_noalloc(const moe_config_t* cfg, const int32_
   const int P = cfg->num_ranks, Tr = cfg->tokens_per_rank, E = cfg->num_experts,
             k = cfg->top_k;
   const long long Na = (long long)P * Tr * k;
-  // Chunking: whole tokens, about 2048 assignments per chunk, never crossing
-  // a source rank.
-  int tpc = 2048 / k;
-  if (tpc < 1) tpc = 1;
-  if (tpc > moe::kMaxChunkAssign / k) tpc = moe::kMaxChunkAssign / k;
-  if (tpc > Tr) tpc = Tr;
+  const int tpc = chunk_tokens(cfg);
   const int cps = (Tr + tpc - 1) / tpc;
   const int nchunks = P * cps;
   // Scratch map: [control words][chunk histograms][source prefixes][codes].
@@ -108,9 +166,12 @@ extern "C" int moe_dispatch_layout_noalloc(const moe_config_t* cfg, const int32_
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  char* base = static_cast<char*>(scratch_address(dev));
-  if (!base) return MOE_ERR_CUDA;
-  if (moe::layout_prepare(E, tpc, k, P) != cudaSuccess) return MOE_ERR_CUDA;
+  const DeviceSetup* ds = device_setup(dev);
+  if (!ds) return MOE_ERR_CUDA;
+  if (moe::layout_smem_bytes(E, tpc, k, P) > ds->layout_dyn_max ||
+      moe::scan_smem_bytes(E, P) > ds->scan_dyn_max)
+    return MOE_ERR_UNSUPPORTED;
+  char* base = static_cast<char*>(ds->scratch);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The scratch keeps the previous call's contents: the control words (status
   // and the chunk arrival counter) must start at zero.

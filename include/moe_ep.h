@@ -52,8 +52,8 @@
  *     stream if that kernel lets its dependents launch before it finishes
  *     (kernels launched without programmatic dependent launch, and this
  *     library's own kernels, are fine).
- *   - Every call that launches work is asynchronous and can be captured in a
- *     CUDA graph. Capture a layout call together with the dispatch that
+ *   - Every call on a handle that launches work is asynchronous and can be
+ *     captured in a CUDA graph. Capture a layout call together with the dispatch that
  *     follows it: the layout records on the host that the per-source tables
  *     are pending, and that dispatch's launch builds them.
  */
@@ -326,22 +326,27 @@ int moe_combine(moe_handle_t h, const void *y, const float *w, void *out,
 
 /* ---- layout without any device allocation -------------------------------
  * The pages have no counterpart for this entry point. It serves callers that
- * may not allocate device memory and have no workspace to hand over: code
- * running while a CUDA graph is being captured, host frameworks whose plugin
- * interface passes only inputs and outputs, processes whose device allocator
- * belongs to someone else. It computes what moe_dispatch_layout computes plus
- * the inverse permutation inv[T*k] (which the workspace path writes during
- * moe_dispatch), from ids int32 [T, k], into the caller's arrays named by
- * *out (every pointer of moe_layout_view_t must be a device array of the size
- * given there). No cudaMalloc, cudaFree or allocating library routine is
- * called. Intermediate data lives in one file-scope device array of
+ * may not allocate device memory and have no workspace to hand over: host
+ * frameworks whose plugin interface passes only inputs and outputs, processes
+ * whose device memory belongs to another allocator (a caching allocator or a
+ * fixed budget that a cudaMalloc of ours would overrun or bypass), and code
+ * that must not let an allocation or a free synchronise the device. It
+ * computes what moe_dispatch_layout computes plus the inverse permutation
+ * inv[T*k] (which the workspace path writes during moe_dispatch), from ids
+ * int32 [T, k], into the caller's arrays named by *out (every pointer of
+ * moe_layout_view_t must be a device array of the size given there). No
+ * cudaMalloc, cudaFree or allocating library routine is called.
+ * Intermediate data lives in one file-scope device array of
  * MOE_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
  * until the process exits; a problem whose scratch (256 + 4*E*P*ceil(T_r/c)
  * + 4*E*(P+1) + 4*T*k bytes, each term rounded up to 256, c = chunk tokens)
- * exceeds it
- * returns MOE_ERR_UNSUPPORTED and enqueues nothing.
- * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
+ * exceeds it, or whose layout tables exceed the layout kernels' shared
+ * memory (as for moe_handle_create), returns MOE_ERR_UNSUPPORTED and
+ * enqueues nothing.
+ * The first call in each device context (the first call on a device, and the
+ * first after that device was reset) does a one-time set-up with that device
+ * current: it looks up the array's device address and raises the layout
+ * kernels' shared-memory limits. Make that first call before any stream
  * capture. Every call shares the array and finds the previous call's
  * contents: each call clears the control words first, and calls that overlap
  * on the GPU (other streams, other threads) race and must be serialised by
