@@ -188,6 +188,36 @@ class MoeLayer:
         main.wait_stream(side)
         return self.out
 
+    def buffers(self) -> dict:
+        """Every row buffer this layer owns, by name (those of the comparators
+        only once they have been allocated by a first use)."""
+        out = {"recv_x": self.recv_x, "y": self.y, "out": self.out}
+        if self.recv_scale is not None:
+            out["recv_scale"] = self.recv_scale
+        out.update({"meta." + k: v for k, v in self.meta.items()})
+        if getattr(self, "send_x", None) is not None:
+            out["send_x"] = self.send_x
+            if self.send_scale is not None:
+                out["send_scale"] = self.send_scale
+        if getattr(self, "gathered_x", None) is not None:
+            out["gathered_x"] = self.gathered_x
+            if self.gathered_scale is not None:
+                out["gathered_scale"] = self.gathered_scale
+        if self.slots is not None:
+            out["slots.x"] = self.slots["x"]
+            out["slots.y"] = self.slots["y"]
+            if self.slots["scale"] is not None:
+                out["slots.scale"] = self.slots["scale"]
+            out.update({"slots.meta." + k: v for k, v in self.slots["meta"].items()})
+        return out
+
+    def poison(self, byte: int = 0xFF) -> None:
+        """Fills every row buffer with one byte value (tests: rows a kernel must
+        not write keep it, rows it must write lose it)."""
+        import torch
+        for t in self.buffers().values():
+            t.view(-1).view(torch.uint8).fill_(byte)
+
     def layout_view(self) -> dict:
         return B.moe_get_layout(self.handle)
 

@@ -79,10 +79,11 @@ def run_gpu(wl: W.Workload, inp: W.Inputs, ids=None, layer=None, stream=None,
     return res
 
 
-def run_oracle(wl: W.Workload, inp: W.Inputs, ids=None, w=None):
-    """The same layer on the CPU oracle. ids/w override the inputs' routing."""
+def run_oracle(wl: W.Workload, inp: W.Inputs, ids=None, w=None, threads: int = 1):
+    """The same layer on the CPU oracle. ids/w override the inputs' routing.
+    threads > 1 runs the oracle's token-independent steps on token ranges."""
     if ids is None and inp.logits is not None:
-        ids, w = oracle.route_topk(inp.logits, wl.k)
+        ids, w = oracle.route_topk(inp.logits, wl.k, threads=threads)
     elif ids is None:
         ids, w = inp.ids, inp.w
     elif w is None:
@@ -91,14 +92,16 @@ def run_oracle(wl: W.Workload, inp: W.Inputs, ids=None, w=None):
     rows = wl.rows_max
     fp8 = wl.dispatch_dtype == W.MOE_FP8_E4M3
     if fp8:
-        recv, sc, meta = oracle.dispatch_fp8(wl.P, wl.Tr, wl.E, wl.k, inp.x, w, ids, lay["inv"], rows)
-        y = oracle.expert_dequant_fp8(recv, sc)
+        recv, sc, meta = oracle.dispatch_fp8(wl.P, wl.Tr, wl.E, wl.k, inp.x, w, ids, lay["inv"],
+                                             rows, threads=threads)
+        y = oracle.expert_dequant_fp8(recv, sc, threads=threads)
     else:
-        recv, meta = oracle.dispatch_bf16(wl.P, wl.Tr, wl.E, wl.k, inp.x, w, ids, lay["inv"], rows)
+        recv, meta = oracle.dispatch_bf16(wl.P, wl.Tr, wl.E, wl.k, inp.x, w, ids, lay["inv"],
+                                          rows, threads=threads)
         sc = None
         c = inp.expert_scale if inp.expert_scale is not None else np.ones(wl.E, np.float32)
         y = oracle.expert_scale_bf16(wl.E, lay["expert_offset"], c, recv)
-    out = oracle.combine(lay["inv"], w, y, wl.T, wl.k)
+    out = oracle.combine(lay["inv"], w, y, wl.T, wl.k, threads=threads)
     return dict(ids=ids, w=w, layout=lay, recv_x=recv, recv_scale=sc, meta=meta, y=y, out=out)
 
 

@@ -27,6 +27,29 @@ def test_full_size_parity(gpu, name):
     assert st["kept"] == wl.Na
 
 
+def test_prefill_full_width_staged_fp8_dispatch_every_element(gpu):
+    """The kernel full-size prefill times: at H = 7168 with at least 16 tokens
+    per dispatch CTA the FP8 dispatch stages each CTA's next token row in
+    shared memory (four 16-value chunks per thread). Prefill's per-token
+    distribution, capacity rule and expert stand-in at 32 x 1300 tokens
+    (332,800 assignments): every receive row, scale, metadata element, expert
+    row and combined row against the oracle."""
+    import os
+
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Tr = 1300
+    wl = W.PREFILL.scaled("prefill_tr1300", Tr=Tr, cap=W.prefill_capacity(32 * Tr, 8, 256))
+    # the launch takes min(T, 16 * SMs) CTAs and stages rows from 16 tokens per CTA
+    assert wl.T >= 16 * 16 * sms and wl.H // 16 > 256
+    inp = W.make_inputs(wl)
+    g = run_gpu(wl, inp)
+    o = run_oracle(wl, inp, threads=os.cpu_count() or 1)
+    st = compare(wl, g, o, routed=True)
+    assert g["status"] == 0
+    assert st["kept"] == int(o["layout"]["totals"][0]) > 0.99 * wl.Na
+
+
 def test_full_size_prefill_sampled(gpu):
     import torch
     wl = W.PREFILL
