@@ -19,10 +19,14 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 // Exclusive scan in place of a[0..n) held in shared memory, by the whole CTA.
-// tmp: 32 ints of shared scratch. Returns the total. Ends with __syncthreads.
+// tmp: 32 ints of shared scratch. Returns the total. Starts and ends with
+// __syncthreads: a thread scans a run of ceil(n / blockDim) elements that
+// other threads may have written just before the call (when n exceeds the
+// thread count the runs are not the elements a thread wrote itself).
 __device__ int cta_exclusive_scan(int* a, int n, int* tmp) {
   const int nt = blockDim.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
   const int per = (n + nt - 1) / nt;
   const int b0 = min(n, (int)threadIdx.x * per), b1 = min(n, b0 + per);
   int local = 0;
