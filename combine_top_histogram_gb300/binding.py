@@ -20,6 +20,7 @@ MOE_FP8_E4M3 = 1
 MOE_STATUS_BAD_EXPERT_ID = 0x1
 MOE_STATUS_TIMEOUT = 0x2
 MOE_STATUS_SLOT_OVERFLOW = 0x4
+MOE_STATUS_BOUNDS = 0x8
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_TOPK = 32
 MOE_MAX_RANKS = 1024
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "moe_dispatch_two_stage", "moe_layout_dispatch_fused", "moe_set_wait_limit",
     "moe_dispatch_tokens", "moe_expert_standin_tokens", "moe_combine_tokens",
     "moe_dispatch_allgather", "moe_layout_tables", "moe_dispatch_fixed_slots",
-    "moe_fixed_slot_rows",
+    "moe_fixed_slot_rows", "moe_debug_bounds",
 )
 
 
@@ -69,6 +70,10 @@ _lock = threading.Lock()
 
 
 def library_path() -> str:
+    """The release library, or with MOE_EP_DEBUG_BOUNDS=1 in the environment
+    the build with device bounds checks (MOE_STATUS_BOUNDS)."""
+    if os.environ.get("MOE_EP_DEBUG_BOUNDS", "") == "1":
+        return _build.DEBUG_LIB_PATH
     return _build.LIB_PATH
 
 
@@ -142,6 +147,8 @@ def load_library():
         lib.moe_copy_d2h_async.argtypes = [vp, vp, sz, vp]
         lib.moe_error_string.restype = ctypes.c_char_p
         lib.moe_error_string.argtypes = [i32]
+        lib.moe_debug_bounds.restype = i32
+        lib.moe_debug_bounds.argtypes = []
         _lib = lib
         return lib
 
@@ -396,3 +403,8 @@ def moe_copy_d2h_async(dst_host, src, stream=None) -> None:
 
 def moe_error_string(code: int) -> str:
     return load_library().moe_error_string(code).decode()
+
+
+def moe_debug_bounds() -> bool:
+    """True if the loaded library checks every computed row index on the device."""
+    return bool(load_library().moe_debug_bounds())

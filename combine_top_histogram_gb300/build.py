@@ -16,9 +16,14 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libmoe_ep.so")
+# The same sources with device bounds checks (MOE_DEBUG_BOUNDS): every row
+# index a kernel computes is checked against its buffer before the access.
+DEBUG_LIB_PATH = os.path.join(BUILD_DIR, "libmoe_ep_debug.so")
 SOURCES = ["api.cu", "layout.cu", "dispatch.cu", "combine.cu", "layout_noalloc.cu", "two_stage.cu",
            "fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+VARIANTS = {"release": ([], BUILD_DIR, LIB_PATH),
+            "debug": (["-DMOE_DEBUG_BOUNDS"], os.path.join(BUILD_DIR, "debug"), DEBUG_LIB_PATH)}
 
 
 def nvcc() -> str:
@@ -33,43 +38,54 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(variant: str = "release") -> bool:
+    lib = VARIANTS[variant][2]
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
+          variants=("release", "debug")) -> str:
+    """Compiles every translation unit of every requested variant in parallel
+    (one nvcc process each), then links one library per variant. Returns the
+    release library's path."""
+    todo = [v for v in variants if force or not up_to_date(v)]
+    if not todo:
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
-             *ARCH]
+    base = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
+            *ARCH]
     if ptxas_v:
-        flags += ["-Xptxas", "-v"]
+        base += ["-Xptxas", "-v"]
     procs = []
-    objs = []
-    for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        objs.append(obj)
-        cmd = [nvcc(), *flags, "-c", os.path.join(CSRC, src), "-o", obj]
-        if verbose:
-            print(" ".join(cmd), file=sys.stderr)
-        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+    objs = {}
+    for v in todo:
+        defs, odir, _ = VARIANTS[v]
+        os.makedirs(odir, exist_ok=True)
+        for src in SOURCES:
+            obj = os.path.join(odir, src.replace(".cu", ".o"))
+            objs.setdefault(v, []).append(obj)
+            cmd = [nvcc(), *base, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
+            if verbose:
+                print(" ".join(cmd), file=sys.stderr)
+            procs.append((f"{v}:{src}",
+                          subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
     failed = []
-    for src, p in procs:
+    for name, p in procs:
         out, _ = p.communicate()
         text = out.decode(errors="replace")
         if p.returncode != 0:
-            failed.append(f"{src}:\n{text}")
+            failed.append(f"{name}:\n{text}")
         elif text.strip() and (verbose or ptxas_v):
             print(text, file=sys.stderr)
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
-    subprocess.check_call([nvcc(), "-shared", *ARCH, "-o", tmp, *objs, "-lcudart"])
-    os.replace(tmp, LIB_PATH)
+    for v in todo:
+        lib = VARIANTS[v][2]
+        tmp = lib + f".{os.getpid()}.tmp"
+        subprocess.check_call([nvcc(), "-shared", *ARCH, "-o", tmp, *objs[v], "-lcudart"])
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -380,6 +380,7 @@ static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void
   }
   a.P = h->cfg.num_ranks;
   a.status = h->status;
+  a.row_limit = fixed ? fixed_slot_rows(&h->cfg) : h->rows_max;
   if (fixed) {
     a.src_pre = h->src_pre;
     a.slot_Tr = h->cfg.tokens_per_rank;
@@ -443,6 +444,8 @@ int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* 
   a.send_pos = h->send_pos;
   a.src_base = h->src_base;
   a.recv_offset = h->recv_offset;
+  a.status = h->status;
+  a.row_limit = h->rows_max;
   rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, st));
   if (rc != MOE_OK) return rc;
   moe::A2avArgs c{};
@@ -459,6 +462,7 @@ int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* 
   c.P = h->cfg.num_ranks;
   c.E = h->cfg.num_experts;
   c.nblk = h->cfg.hidden / 128;
+  c.status = h->status;
   rc = cuda_rc(moe::launch_a2av(c, h->num_sms, st));
   if (rc == MOE_OK) {
     h->dispatch_gen = h->layout_gen;
@@ -517,6 +521,8 @@ int moe_dispatch_allgather(moe_handle_t h, const void* x, const float* w, void* 
   a.cps = h->cur_cps;
   a.nchunks = h->cfg.num_ranks * h->cur_cps;
   a.cap = h->cfg.expert_capacity;
+  a.status = h->status;
+  a.row_limit = h->rows_max;
   g.gathered = gathered_x;
   g.gathered_scale = gathered_scale;
   g.P = h->cfg.num_ranks;
@@ -599,6 +605,8 @@ int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids,
   a.cps = cps;
   a.nchunks = P * cps;
   a.cap = h->cfg.expert_capacity;
+  a.status = h->status;
+  a.row_limit = h->rows_max;
   f.bar = h->status + 4;
   f.wait_limit = h->wait_limit;
   f.prefetch_x = prefetch ? 1 : 0;
@@ -631,6 +639,7 @@ int moe_expert_standin(moe_handle_t h, const void* recv_x, const float* recv_sca
   a.E = h->cfg.num_experts;
   a.H = h->cfg.hidden;
   a.fp8 = fp8 ? 1 : 0;
+  a.status = h->status;
   if (h->fixed_rows) {  // the filled rows of every slot region, found through inv
     a.inv = h->inv;
     a.a0 = 0;
@@ -656,6 +665,8 @@ static int combine_range(moe_handle_t h, long long g0, long long g1, const void*
   a.g0 = g0;
   a.k = h->cfg.top_k;
   a.H = h->cfg.hidden;
+  a.row_limit = h->fixed_rows ? fixed_slot_rows(&h->cfg) : h->rows_max;
+  a.status = h->status;
   return cuda_rc(moe::launch_combine(a, h->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
@@ -694,6 +705,7 @@ int moe_expert_standin_tokens(moe_handle_t h, int64_t token_begin, int64_t token
   a.E = h->cfg.num_experts;
   a.H = h->cfg.hidden;
   a.fp8 = fp8 ? 1 : 0;
+  a.status = h->status;
   if (h->fixed_rows) a.slot_rows = (long long)h->cfg.num_ranks * h->cfg.tokens_per_rank;
   return cuda_rc(moe::launch_standin_tokens(a, h->num_sms, static_cast<cudaStream_t>(stream)));
 }
@@ -720,6 +732,14 @@ int moe_copy_d2h_async(void* dst_host, const void* src_device, size_t bytes, voi
   if (!bytes) return MOE_OK;
   return cuda_rc(cudaMemcpyAsync(dst_host, src_device, bytes, cudaMemcpyDeviceToHost,
                                  static_cast<cudaStream_t>(stream)));
+}
+
+int moe_debug_bounds(void) {
+#ifdef MOE_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 const char* moe_error_string(int code) {

@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kCombineThreads) k_combine(const CombineArgs p
     int* rows_s = rows_buf[par];
     float* w_s = w_buf[par];
     if (tid < k) {
-      rows_s[tid] = __ldg(p.inv + g * k + tid);
+      const int r = __ldg(p.inv + g * k + tid);
+      rows_s[tid] = (r >= 0 && row_ok(r, p.row_limit, p.status)) ? r : -1;
       w_s[tid] = __ldg(p.w + g * k + tid);
     }
     __syncthreads();
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(128) k_standin(const StandinArgs p) {
   pdl_wait();
   pdl_trigger();
   const int total = __ldg(p.expert_offset + p.E);
+  if (total > 0 && blockIdx.x == 0 && threadIdx.x == 0) row_ok(total - 1, p.rows_max, p.status);
   for (long long r = blockIdx.x; r < total && r < p.rows_max; r += gridDim.x) {
     if (threadIdx.x == 0) {
       int lo = 0, hi = p.E - 1;  // largest e with expert_offset[e] <= r
@@ -188,7 +190,9 @@ __global__ void __launch_bounds__(128) k_standin_tokens(const StandinArgs p) {
   pdl_trigger();
   for (long long a = p.a0 + blockIdx.x; a < p.a1; a += gridDim.x) {
     if (threadIdx.x == 0) {
-      const int r = __ldg(p.inv + a);
+      int r = __ldg(p.inv + a);
+      const long long limit = p.slot_rows > 0 ? p.slot_rows * p.E : p.rows_max;
+      if (r >= 0 && !row_ok(r, limit, p.status)) r = -1;
       r_s = r;
       if (r >= 0) {
         int lo = 0, hi = p.E - 1;  // largest e with expert_offset[e] <= r

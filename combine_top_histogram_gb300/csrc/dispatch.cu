@@ -80,7 +80,10 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
   const long long a = g * p.k + j;
   const int code = in.code;
   int r = -1;
-  if (code >= 0) {
+  // (debug bounds build: an assignment code naming no expert, or a chunk
+  // outside the table, is skipped like a row outside its buffer)
+  if (code >= 0 && row_ok(code_expert(code), p.E, p.status) &&
+      row_ok((g / p.Tr) * p.cps + (g % p.Tr) / p.tpc, p.nchunks, p.status)) {
     const int e = code_expert(code);
     const int s = (int)(g / p.Tr);
     const int t = (int)(g - (long long)s * p.Tr);
@@ -92,11 +95,14 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
     if (p.slot_Tr > 0 && q >= p.slot_Tr) atomicOr(p.status, MOE_STATUS_SLOT_OVERFLOW);
     if ((p.cap <= 0 || pos < p.cap) && q < max(p.slot_Tr, 1)) {
       r = p.slot_Tr > 0 ? (e * p.P + s) * p.slot_Tr + q : __ldg(p.expert_offset + e) + pos;
-      p.m_local_expert[r] = e % p.L;
-      p.m_src_rank[r] = s;
-      p.m_src_token[r] = t;
-      p.m_slot[r] = j;
-      p.m_weight[r] = in.w;
+      if (!row_ok(r, p.row_limit, p.status)) r = -1;
+      if (r >= 0) {
+        p.m_local_expert[r] = e % p.L;
+        p.m_src_rank[r] = s;
+        p.m_src_token[r] = t;
+        p.m_slot[r] = j;
+        p.m_weight[r] = in.w;
+      }
     }
   }
   p.inv[a] = r;
@@ -105,6 +111,7 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
   if (p.send_pos && r >= 0) {
     const long long se = (long long)code_expert(code) + (long long)(g / p.Tr) * p.E;
     dst = __ldg(p.src_base + g / p.Tr) + __ldg(p.send_pos + se) + (r - __ldg(p.recv_offset + se));
+    if (!row_ok(dst, p.row_limit, p.status)) dst = -1;
   }
   rows_s[j] = dst;
 }

@@ -140,10 +140,10 @@ __device__ __forceinline__ bool fused_body(const FusedArgs& f, int* smem) {
       const long long a = a0 + i;
       const int code = __ldcg(p.acode + a);
       int r = -1;
-      if (code >= 0) {
+      if (code >= 0 && row_ok(code_expert(code), p.E, p.status)) {
         const int e = code_expert(code);
         const int pos = __ldcg(p.hist + (long long)e * p.nchunks + b) + code_rank(code);
-        if (p.cap <= 0 || pos < p.cap) {
+        if ((p.cap <= 0 || pos < p.cap) && row_ok(eoff[e] + pos, d.row_limit, p.status)) {
           r = eoff[e] + pos;
           const int t = t0 + i / p.k;
           d.m_local_expert[r] = e % p.L;

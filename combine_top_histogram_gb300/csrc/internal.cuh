@@ -111,7 +111,8 @@ struct DispatchArgs {
   // assignments to e; src_pre gives the prefix at s's first chunk.
   const int32_t* src_pre;
   int slot_Tr, P;
-  uint32_t* status;       // MOE_STATUS_SLOT_OVERFLOW (fixed slots)
+  uint32_t* status;       // MOE_STATUS_SLOT_OVERFLOW (fixed slots), MOE_STATUS_BOUNDS
+  long long row_limit;    // rows of the destination buffer (debug bounds checks)
 };
 
 // Persistent single-launch route/layout/dispatch (fused.cu).
@@ -145,6 +146,7 @@ struct A2avArgs {
   long long rows_max;
   long long row_bytes;       // payload bytes per row (multiple of 16)
   int P, E, nblk;
+  uint32_t* status;          // MOE_STATUS_BOUNDS (debug bounds checks)
 };
 
 struct CombineArgs {
@@ -155,6 +157,8 @@ struct CombineArgs {
   long long T;            // tokens [g0, T) are combined (g0 = 0: all)
   long long g0;
   int k, H;
+  long long row_limit;    // rows of y (debug bounds checks)
+  uint32_t* status;       // MOE_STATUS_BOUNDS (debug bounds checks)
 };
 
 struct StandinArgs {
@@ -169,7 +173,28 @@ struct StandinArgs {
   long long rows_max;
   int E, H, fp8;
   long long slot_rows;     // fixed-slot layout: rows per expert region (P*T_r); 0 = compact
+  uint32_t* status;        // MOE_STATUS_BOUNDS (debug bounds checks)
 };
+
+// Debug bounds build (compiled with -DMOE_DEBUG_BOUNDS): a row index r that a
+// kernel computed is checked against the row count of the buffer it indexes
+// before any access through it; outside [0, limit) it sets MOE_STATUS_BOUNDS
+// and the caller skips the access. Without the flag this is the constant true
+// and the checks compile to nothing. Callers pass only r >= 0 (-1 already
+// means "no row").
+__device__ __forceinline__ bool row_ok(long long r, long long limit, uint32_t* status) {
+#ifdef MOE_DEBUG_BOUNDS
+  if (r < 0 || r >= limit) {
+    if (status) atomicOr(status, MOE_STATUS_BOUNDS);
+    return false;
+  }
+#else
+  (void)r;
+  (void)limit;
+  (void)status;
+#endif
+  return true;
+}
 
 // Programmatic dependent launch: every kernel of the path is launched with
 // programmatic stream serialization, waits for its predecessor grid

@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(128) k_a2av(const A2avArgs p) {
     }
     __syncthreads();
     const long long sr = src_row_s;
+    if (!row_ok(sr, p.rows_max, p.status) || !row_ok(r, p.rows_max, p.status)) {
+      __syncthreads();
+      continue;  // debug bounds build only: a send or receive row outside the pool
+    }
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.send) +
                                                       sr * p.row_bytes);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.recv) + r * p.row_bytes);

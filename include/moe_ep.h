@@ -92,6 +92,9 @@ extern "C" {
 #define MOE_STATUS_SLOT_OVERFLOW 0x4u  /* fixed slots: more than T_r assignments of one
                                           source to one expert (an id repeated within a
                                           token); the excess is not written, inv = -1 */
+#define MOE_STATUS_BOUNDS 0x8u         /* debug bounds build only (moe_debug_bounds()):
+                                          a computed row index fell outside its buffer;
+                                          that access was skipped (and inv = -1) */
 
 /* Problem description. Passed by pointer; copied into the handle. */
 typedef struct {
@@ -388,6 +391,15 @@ int moe_combine_tokens(moe_handle_t h, int64_t token_begin, int64_t token_end, c
  * status word. Synchronises `stream`: tests and debugging only. *flags
  * receives MOE_STATUS_* bits. */
 int moe_read_status(moe_handle_t h, uint32_t *flags, void *stream);
+
+/* Housekeeping (no counterpart on the pages): 1 if this library was built
+ * with device bounds checks (compiled with MOE_DEBUG_BOUNDS; built beside the
+ * release library as libmoe_ep_debug.so). In that build every row index a
+ * kernel computes (receive, send-pool, slot, expert-output and restored rows,
+ * and the scale and metadata entries of a row) is checked against its
+ * buffer's row count before the access; an index outside it sets
+ * MOE_STATUS_BOUNDS and the access is skipped. 0 for the release build. */
+int moe_debug_bounds(void);
 
 /* Human-readable name of a MOE_ERR_* code (static string). */
 const char *moe_error_string(int code);

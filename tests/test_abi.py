@@ -29,6 +29,18 @@ def test_library_exports_every_declared_symbol(cuda_lib):
     assert set(declared_functions()) <= exported
 
 
+def test_debug_build_exports_the_same_symbols_and_reports_its_checks(cuda_lib):
+    import importlib
+    build = importlib.import_module("combine_top_histogram_gb300.build")
+    build.build(variants=("debug",))
+    out = os.popen(f"nm -D --defined-only {build.DEBUG_LIB_PATH}").read()
+    exported = set(re.findall(r"\bT (moe_[a-z_0-9]+)", out))
+    assert set(declared_functions()) <= exported
+    dbg = ctypes.CDLL(build.DEBUG_LIB_PATH)
+    assert dbg.moe_debug_bounds() == 1
+    assert cuda_lib.moe_debug_bounds() == 0
+
+
 def test_host_only_sizing_and_validation(cuda_lib):
     cfg = B.make_config(8, 128, 256, 8, 7168)
     assert B.moe_recv_rows_max(cfg) == 8 * 128 * 8
