@@ -70,8 +70,11 @@ _lock = threading.Lock()
 
 
 def library_path() -> str:
-    """The release library, or with MOE_EP_DEBUG_BOUNDS=1 in the environment
-    the build with device bounds checks (MOE_STATUS_BOUNDS)."""
+    """The release library; with MOE_EP_DEBUG_BOUNDS=1 in the environment the
+    build with device bounds checks (MOE_STATUS_BOUNDS); with MOE_EP_LIBRARY
+    set, that file (another build of the same sources)."""
+    if os.environ.get("MOE_EP_LIBRARY"):
+        return os.environ["MOE_EP_LIBRARY"]
     if os.environ.get("MOE_EP_DEBUG_BOUNDS", "") == "1":
         return _build.DEBUG_LIB_PATH
     return _build.LIB_PATH

@@ -43,7 +43,7 @@ int validate(const moe_config_t* c) {
 
 struct Plan {
   int tpc_route, cps_route, tpc_ids, cps_ids, nchunks_max;
-  size_t off_ctrl, off_acc, off_totals, off_n_raw, off_n_kept, off_eoff, off_cnt, off_kept, off_C,
+  size_t off_ctrl, off_acc, off_acc_se, off_totals, off_n_raw, off_n_kept, off_eoff, off_cnt, off_kept, off_C,
       off_send, off_recv, off_rank, off_hist, off_pre, off_acode, off_inv, off_spos, off_sbase,
       bytes;
 };
@@ -88,6 +88,7 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   };
   p.off_ctrl = take(64);
   p.off_acc = take((size_t)E * 4);
+  p.off_acc_se = take((size_t)P * E * 4);
   p.off_totals = take(4 * sizeof(int32_t));
   p.off_n_raw = take((size_t)E * 4);
   p.off_n_kept = take((size_t)E * 4);
@@ -182,6 +183,50 @@ long long fixed_slot_rows(const moe_config_t* c) {
   return rows;
 }
 
+// The direct dispatch (no scan kernel between the layout and the dispatch)
+// pays off for small, latency-bound layers (decode): per token it sums the
+// per-(source, expert) totals of earlier sources and the source's earlier
+// chunk counts, and each tables CTA sums the totals of earlier sources, so
+// the sources and chunks are bounded; and its token's codes can only be read
+// after the wait, which costs a CTA that copies several tokens more than the
+// scan kernel saves, so it is used when every dispatch CTA copies one token
+// (T <= 16 CTAs per SM).
+constexpr int kDirectMaxRanks = 32;
+constexpr int kDirectMaxChunks = 256;
+
+// Lanes that sum one slot's earlier counts: a power of two up to 32 such that
+// all k slots fit in the dispatch CTA's 128 threads.
+int direct_group(int k) {
+  int G = 32;
+  while (G > 1 && G * k > 128) G >>= 1;
+  return G;
+}
+
+// Launches the scan kernel for a layout that was laid out for the direct
+// dispatch but is needed in scanned form (any other consumer): with the totals
+// still pending it consumes and clears them; after a direct dispatch (totals
+// already cleared) it rebuilds the per-expert arrays from the chunk counts
+// with the arrival counter instead.
+int ensure_scanned(moe_handle_t h, cudaStream_t st) {
+  if (h->scan_state == 0) return MOE_OK;
+  moe::LayoutArgs a = layout_args(h, false);
+  a.tpc = h->cur_tpc;
+  a.cps = h->cur_cps;
+  a.nchunks = h->cfg.num_ranks * h->cur_cps;
+  if (h->scan_state == 1) {
+    a.acc_se = h->acc_se;  // cleared with the per-expert totals
+  } else {
+    a.acc_add = nullptr;   // arrival-counter form; the last CTA writes the offsets
+  }
+  const int rc = cuda_rc(moe::launch_scan(a, st));
+  if (rc != MOE_OK) {
+    h->acc_dirty = 1;
+    return rc;
+  }
+  h->scan_state = 0;
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -261,8 +306,12 @@ int moe_handle_create(const moe_config_t* cfg, void* d_workspace, size_t bytes,
   h->src_base = reinterpret_cast<int32_t*>(ws + p.off_sbase);
   h->wait_limit = 1ll << 22;  // ~0.3 s of 64 ns polls
   h->acc = reinterpret_cast<int32_t*>(ws + p.off_acc);
+  h->acc_se = reinterpret_cast<int32_t*>(ws + p.off_acc_se);
+  h->direct_ok = cfg->num_ranks <= kDirectMaxRanks && h->T <= 16ll * sms;
   if (cudaMemset(ws + p.off_ctrl, 0, 64) != cudaSuccess ||
-      cudaMemset(ws + p.off_acc, 0, (size_t)cfg->num_experts * 4) != cudaSuccess) {
+      cudaMemset(ws + p.off_acc, 0, (size_t)cfg->num_experts * 4) != cudaSuccess ||
+      cudaMemset(ws + p.off_acc_se, 0, (size_t)cfg->num_ranks * cfg->num_experts * 4) !=
+          cudaSuccess) {
     free(h);
     return MOE_ERR_CUDA;
   }
@@ -284,17 +333,26 @@ int moe_route_topk(moe_handle_t h, const float* logits, int32_t* ids, float* w, 
 static int run_layout(moe_handle_t h, bool route, const int32_t* ids_in, const float* logits,
                       int32_t* ids_out, float* w_out, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (h->acc_dirty) {  // a failed launch may have left partial totals
-    if (cudaMemsetAsync(h->acc, 0, (size_t)h->cfg.num_experts * 4, st) != cudaSuccess)
+  // A failed launch may have left partial totals, and a layout laid out for
+  // the direct dispatch that nothing consumed leaves its totals behind.
+  if (h->acc_dirty || h->scan_state == 1) {
+    if (cudaMemsetAsync(h->acc, 0, (size_t)h->cfg.num_experts * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(h->acc_se, 0, (size_t)h->cfg.num_ranks * h->cfg.num_experts * 4, st) !=
+            cudaSuccess)
       return MOE_ERR_CUDA;
     h->acc_dirty = 0;
+    h->scan_state = 0;
   }
   moe::LayoutArgs a = layout_args(h, route);
   a.ids_in = ids_in;
   a.logits = logits;
   a.ids_out = ids_out;
   a.w_out = w_out;
-  const int rc = cuda_rc(moe::launch_layout(a, route, h->num_sms, st));
+  // small layouts: only the layout kernel; the dispatch lays itself out from
+  // the totals (direct dispatch), and any other consumer scans first
+  const bool direct = h->direct_ok && a.nchunks <= kDirectMaxChunks;
+  if (direct) a.acc_se = h->acc_se;
+  const int rc = cuda_rc(moe::launch_layout(a, route, h->num_sms, st, !direct));
   if (rc != MOE_OK) {
     h->acc_dirty = 1;
     return rc;
@@ -303,6 +361,7 @@ static int run_layout(moe_handle_t h, bool route, const int32_t* ids_in, const f
   h->cur_cps = a.cps;
   h->layout_gen += 1;
   h->tables_pending = 1;
+  h->scan_state = direct ? 1 : 0;
   return MOE_OK;
 }
 
@@ -320,6 +379,8 @@ int moe_route_dispatch_layout(moe_handle_t h, const float* logits, int32_t* ids,
 int moe_layout_tables(moe_handle_t h, void* stream) {
   if (!h) return MOE_ERR_INVALID_ARG;
   if (h->layout_gen == 0) return MOE_ERR_STATE;
+  const int rc = ensure_scanned(h, static_cast<cudaStream_t>(stream));
+  if (rc != MOE_OK) return rc;
   return ensure_tables(h, static_cast<cudaStream_t>(stream));
 }
 
@@ -349,6 +410,14 @@ static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void
   if (fp8 && !recv_scale) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(recv_x, 16)) return MOE_ERR_INVALID_ARG;
   if (h->layout_gen == 0) return MOE_ERR_STATE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the whole layer into the compact receive rows right after a layout laid
+  // out for it: the direct dispatch; anything else needs the scanned layout
+  const bool direct = !fixed && g0 == 0 && g1 == h->T && h->scan_state == 1;
+  if (!direct) {
+    const int rc = ensure_scanned(h, st);
+    if (rc != MOE_OK) return rc;
+  }
   moe::DispatchArgs a{};
   a.x = static_cast<const uint16_t*>(x);
   a.w = w;
@@ -385,11 +454,29 @@ static int dispatch_range(moe_handle_t h, long long g0, long long g1, const void
     a.src_pre = h->src_pre;
     a.slot_Tr = h->cfg.tokens_per_rank;
   }
-  const int rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
+  if (direct) {
+    a.direct = 1;
+    a.direct_G = direct_group(a.k);
+    a.acc = h->acc;
+    a.acc_se = h->acc_se;
+    a.arrive = h->status + 2;
+    a.n_raw = h->n_raw;
+    a.n_kept = h->n_kept;
+    a.expert_offset_out = h->expert_offset;
+    a.rank_base = h->rank_base;
+    a.totals = h->totals;
+    a.Na = h->Na;
+    a.tab = tables_args(h);  // the per-source tables, from the totals
+    a.tab_ctas = h->cfg.num_ranks;
+  }
+  const int rc = cuda_rc(moe::launch_dispatch(a, fp8, h->num_sms, st));
   if (rc == MOE_OK) {
     h->dispatch_gen = h->layout_gen;
     h->tables_pending = 0;
     h->fixed_rows = fixed ? 1 : 0;
+    if (direct) h->scan_state = 2;
+  } else if (direct) {
+    h->acc_dirty = 1;
   }
   return rc;
 }
@@ -412,7 +499,9 @@ int moe_dispatch_two_stage(moe_handle_t h, const void* x, const float* w, void* 
   if (!aligned(x, 16) || !aligned(recv_x, 16) || !aligned(send_x, 16)) return MOE_ERR_INVALID_ARG;
   if (h->layout_gen == 0) return MOE_ERR_STATE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc = ensure_tables(h, st);  // the send positions come from kept_cnt
+  int rc = ensure_scanned(h, st);
+  if (rc != MOE_OK) return rc;
+  rc = ensure_tables(h, st);  // the send positions come from kept_cnt
   if (rc != MOE_OK) return rc;
   rc = cuda_rc(moe::launch_send_pos(h->kept_cnt, h->send_pos, h->src_base,
                                     h->cfg.num_ranks, h->cfg.num_experts, st));
@@ -526,7 +615,9 @@ int moe_dispatch_allgather(moe_handle_t h, const void* x, const float* w, void* 
   g.gathered = gathered_x;
   g.gathered_scale = gathered_scale;
   g.P = h->cfg.num_ranks;
-  int rc = ensure_tables(h, static_cast<cudaStream_t>(stream));
+  int rc = ensure_scanned(h, static_cast<cudaStream_t>(stream));
+  if (rc != MOE_OK) return rc;
+  rc = ensure_tables(h, static_cast<cudaStream_t>(stream));
   if (rc != MOE_OK) return rc;
   rc = cuda_rc(moe::launch_allgather(g, fp8, h->num_sms, static_cast<cudaStream_t>(stream)));
   if (rc == MOE_OK) {
@@ -611,8 +702,10 @@ int moe_layout_dispatch_fused(moe_handle_t h, const float* logits, int32_t* ids,
   f.wait_limit = h->wait_limit;
   f.prefetch_x = prefetch ? 1 : 0;
   f.xs_offset_ints = xs_off;
+  if (h->scan_state == 1) h->acc_dirty = 1;  // a layout whose totals nothing consumed
   const int rc = cuda_rc(moe::launch_fused(f, route, fp8, grid, smem, static_cast<cudaStream_t>(stream)));
   if (rc != MOE_OK) return rc;
+  h->scan_state = 0;
   h->cur_tpc = tpc;
   h->cur_cps = cps;
   h->layout_gen += 1;

@@ -55,11 +55,11 @@ __global__ void __launch_bounds__(kDispatchThreads) k_tables(const TablesArgs t)
   source_tables(t, blockIdx.x, tab_s);
 }
 
-// The assignment code and weight of slot j = threadIdx.x of token g. The
-// codes come from the layout kernel, which is at least two launches before
-// any dispatch (the scan sits between them), so under the launch rule above
-// they are complete when the dispatch starts; the weights are an input, like
-// x. Both may therefore be loaded before the dispatch's wait.
+// The assignment code and weight of slot j = threadIdx.x of token g. With
+// the scan kernel between the layout and the dispatch, the codes (and routed
+// weights) come from a launch at least two before, so under the launch rule
+// above they are complete when the dispatch starts and may be loaded before
+// its wait; in direct mode (no scan kernel) they are loaded after it.
 struct SlotIn {
   int code;
   float w;
@@ -116,22 +116,208 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
   rows_s[j] = dst;
 }
 
-template <int VPT>
+// ---- direct mode ----------------------------------------------------------
+// Small, latency-bound layouts (decode) skip the scan kernel: the dispatch
+// follows the layout kernel directly. A slot's receive row is
+//   (kept assignments to experts before e) + (assignments to e from earlier
+//   sources) + (from the source's earlier chunks) + chunk-local rank,
+// from the per-expert totals acc, the per-(source, expert) totals acc_se and
+// the raw chunk counts in hist that the layout kernel left: every CTA scans the
+// per-expert totals into expert offsets in shared memory, and direct_G lanes
+// sum each slot's other terms in one round trip. The launch's first P CTAs
+// build the per-source tables the same way (CTA 0 also the per-expert arrays).
+//
+// Dynamic shared memory of a direct-mode CTA (ints): eoff[E+1] | tmp[32] |
+// red[2] | (tables CTAs) sk[E + 32].
+__host__ __device__ constexpr int direct_smem_ints(int E) { return (E + 1) + 32 + 2 + (E + 32); }
+
+// Expert offsets of the layout in eoff[0..E] (kept counts, capacity applied,
+// scanned in global expert order); the writer CTA also stores n_raw, n_kept,
+// expert_offset, rank_base and the layer totals.
+__device__ void direct_offsets(const DispatchArgs& p, int* dsm, bool writer) {
+  const int E = p.E, tid = threadIdx.x, NT = blockDim.x;
+  int* eoff = dsm;
+  int* tmp = eoff + E + 1;
+  int* red = tmp + 32;
+  if (tid < 2) red[tid] = 0;
+  int dr = 0, rw = 0;
+  for (int e = tid; e < E; e += NT) {
+    const int raw = __ldcg(p.acc + e);
+    const int kept = (p.cap > 0 && raw > p.cap) ? p.cap : raw;
+    eoff[e] = kept;
+    if (writer) {
+      p.n_raw[e] = raw;
+      p.n_kept[e] = kept;
+    }
+    rw += raw;
+    dr += raw - kept;
+  }
+  __syncthreads();
+  if (writer) {
+    if (dr) atomicAdd(&red[0], dr);
+    if (rw) atomicAdd(&red[1], rw);
+  }
+  const int total = cta_exclusive_scan(eoff, E, tmp);
+  if (tid == 0) eoff[E] = total;
+  if (writer) {
+    for (int e = tid; e <= E; e += NT) p.expert_offset_out[e] = e < E ? eoff[e] : total;
+    for (int d = tid; d <= p.P; d += NT) p.rank_base[d] = d < p.P ? eoff[d * p.L] : total;
+    if (tid == 0) {
+      p.totals[0] = total;
+      p.totals[1] = red[0];
+      p.totals[2] = (int)(p.Na - (long long)red[1]);
+      p.totals[3] = 0;
+    }
+  }
+  __syncthreads();
+}
+
+// Every CTA of a direct-mode launch counts itself out on the arrival counter
+// once it has read the totals for the last time (thread 0's atomic, whose
+// ticket it keeps); the CTA that counted out last clears the totals and the
+// counter for the next layout, after its own work.
+__device__ __forceinline__ unsigned direct_count_out(const DispatchArgs& p) {
+  return threadIdx.x == 0 ? atomicAdd(p.arrive, 1u) : 0u;
+}
+__device__ void direct_end(const DispatchArgs& p, unsigned ticket) {
+  __shared__ unsigned s_ticket;
+  __syncthreads();
+  if (threadIdx.x == 0) s_ticket = ticket;
+  __syncthreads();
+  if (s_ticket != gridDim.x - 1) return;
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) p.acc[e] = 0;
+  for (int i = threadIdx.x; i < p.P * p.E; i += blockDim.x) p.acc_se[i] = 0;
+  if (threadIdx.x == 0) *p.arrive = 0u;
+}
+
+// The code of the slot whose terms this thread helps to sum (direct_G lanes
+// per slot).
+__device__ __forceinline__ int load_group_code(const DispatchArgs& p, long long g) {
+  const int jt = threadIdx.x / p.direct_G;
+  return jt < p.k ? __ldg(p.acode + g * p.k + jt) : -1;
+}
+
+// pre[j] = assignments to slot j's expert that precede token g's chunk: those
+// of earlier sources (acc_se) and of the source's earlier chunks (raw hist),
+// summed over direct_G lanes. Every thread of the CTA takes part (warp-wide
+// shuffles).
+__device__ __forceinline__ void direct_slot_bases(const DispatchArgs& p, long long g, int code,
+                                                  int* pre) {
+  const int G = p.direct_G, jt = threadIdx.x / G, li = threadIdx.x - jt * G;
+  int sp = 0;
+  if (jt < p.k && code >= 0 && row_ok(code_expert(code), p.E, p.status)) {
+    const int e = code_expert(code);
+    const int s = (int)(g / p.Tr);
+    const int bs = (int)(g - (long long)s * p.Tr) / p.tpc;  // chunk within the source
+    for (int s2 = li; s2 < s; s2 += G) sp += __ldcg(p.acc_se + (long long)s2 * p.E + e);
+    const int32_t* col = p.hist + (long long)e * p.nchunks + (long long)s * p.cps;
+    for (int c = li; c < bs; c += G) sp += __ldcg(col + c);
+  }
+  for (int o = G >> 1; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
+  if (li == 0 && jt < p.k) pre[jt] = sp;
+}
+
+// resolve_rows for direct mode: the row of slot j is eoff[e] + pos with
+// pos = pre[j] + rank, kept iff pos is below the capacity.
+__device__ __forceinline__ void resolve_rows_direct(const DispatchArgs& p, long long g,
+                                                    int* rows_s, SlotIn in, const int* eoff,
+                                                    const int* pre) {
+  const int j = threadIdx.x;
+  if (j >= p.k) return;
+  const long long a = g * p.k + j;
+  const int code = in.code;
+  int r = -1;
+  if (code >= 0 && row_ok(code_expert(code), p.E, p.status)) {
+    const int e = code_expert(code);
+    const int pos = pre[j] + code_rank(code);
+    if (p.cap <= 0 || pos < p.cap) {
+      r = eoff[e] + pos;
+      if (!row_ok(r, p.row_limit, p.status)) r = -1;
+      if (r >= 0) {
+        const int s = (int)(g / p.Tr);
+        p.m_local_expert[r] = e % p.L;
+        p.m_src_rank[r] = s;
+        p.m_src_token[r] = (int)(g - (long long)s * p.Tr);
+        p.m_slot[r] = j;
+        p.m_weight[r] = in.w;
+      }
+    }
+  }
+  p.inv[a] = r;
+  rows_s[j] = r;
+}
+
+// The k receive rows of token g into rows_s (either mode); the caller ends
+// with a barrier before reading rows_s. code: load_group_code's value; eoff:
+// the direct mode's expert offsets in shared memory (direct_offsets).
+template <bool DIRECT>
+__device__ __forceinline__ void resolve_token(const DispatchArgs& p, long long g, int* rows_s,
+                                              SlotIn in, int code, const int* eoff) {
+  if (DIRECT) {
+    __shared__ int pre[MOE_MAX_TOPK];
+    direct_slot_bases(p, g, code, pre);
+    __syncthreads();
+    resolve_rows_direct(p, g, rows_s, in, eoff, pre);
+  } else {
+    resolve_rows(p, g, rows_s, in);
+  }
+}
+
+// Direct mode, source s = blockIdx.x < P: the per-source tables from the
+// totals (a = assignments to e from earlier sources, c = from s itself), as
+// source_tables derives them from the scanned prefixes; CTA 0 writes the
+// per-expert arrays too.
+__device__ void direct_tables_cta(const DispatchArgs& p, int* dsm) {
+  pdl_wait();
+  pdl_trigger();
+  direct_offsets(p, dsm, blockIdx.x == 0);
+  const int E = p.E, s = blockIdx.x;
+  const int* eoff = dsm;
+  int* sk = dsm + (E + 1) + 32 + 2;
+  const long long row = (long long)s * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int a = 0;
+    for (int s2 = 0; s2 < s; ++s2) a += __ldcg(p.acc_se + (long long)s2 * E + e);
+    const int c = __ldcg(p.acc_se + row + e);
+    const int kept = p.cap > 0 ? min(max(p.cap - a, 0), c) : c;
+    p.tab.cnt[row + e] = c;
+    p.tab.kept_cnt[row + e] = kept;
+    p.tab.recv_offset[row + e] = eoff[e] + (p.cap > 0 ? min(a, p.cap) : a);
+    sk[e] = kept;
+  }
+  const int total = cta_exclusive_scan(sk, E, sk + E);  // barriers: all reads above are done
+  const unsigned ticket = direct_count_out(p);
+  for (int d = threadIdx.x; d < p.P; d += blockDim.x) {
+    const int lo = sk[d * p.L];
+    const int hi = d + 1 < p.P ? sk[(d + 1) * p.L] : total;
+    p.tab.send_offset[(long long)s * p.P + d] = lo;
+    p.tab.C[(long long)s * p.P + d] = hi - lo;
+  }
+  direct_end(p, ticket);
+}
+
+template <int VPT, bool DIRECT>
 __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const DispatchArgs p) {
   // the k receive rows of the current token; two buffers, alternating per token
   __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  extern __shared__ int dsm[];  // tables CTAs and direct mode
   int par = 0;
   const int nvec = p.H >> 3;  // 16-byte vectors per row
   const int tid = threadIdx.x;
-  bool waited = false;
+  bool waited = false, offsets_done = false;
+  unsigned ticket = 0u;
   if ((int)blockIdx.x < p.tab_ctas) {
-    tables_cta(p);
+    if (DIRECT) direct_tables_cta(p, dsm);
+    else tables_cta(p);
     return;
   }
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
-    const SlotIn si = load_slot(p, g);
+    // direct mode: the layout kernel is the launch just before, so its codes
+    // (and routed weights) are read only after the wait
+    SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
+    int gcode = -1;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -147,7 +333,14 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
           pdl_trigger();
           waited = true;
         }
-        resolve_rows(p, g, rows_s, si);
+        if (DIRECT) {  // the slot loads and (first token) the totals' loads in flight together
+          si = load_slot(p, g);
+          gcode = load_group_code(p, g);
+          if (!offsets_done) direct_offsets(p, dsm, false);
+          offsets_done = true;
+        }
+        resolve_token<DIRECT>(p, g, rows_s, si, gcode, dsm);
+        if (DIRECT && g + nb >= p.T) ticket = direct_count_out(p);  // last read of the totals
         __syncthreads();
       }
       for (int j = 0; j < p.k; ++j) {
@@ -163,28 +356,35 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
     }
     par ^= 1;  // token n+2 rewrites this buffer only after token n+1's barrier
   }
+  if (DIRECT) direct_end(p, ticket);
 }
 
 // FP8: a 128-channel block is 16 consecutive vectors, held by 16 consecutive
 // lanes (blockDim and the vector stride are multiples of 16), so the block's
 // amax is a 4-step xor-shuffle reduction inside each half-warp.
-template <int VPT>
+template <int VPT, bool DIRECT>
 __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const DispatchArgs p) {
   // the k receive rows of the current token; two buffers, alternating per token
   __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  extern __shared__ int dsm[];  // tables CTAs and direct mode
   int par = 0;
   const int nvec = p.H >> 3;
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
-  bool waited = false;
+  bool waited = false, offsets_done = false;
+  unsigned ticket = 0u;
   if ((int)blockIdx.x < p.tab_ctas) {
-    tables_cta(p);
+    if (DIRECT) direct_tables_cta(p, dsm);
+    else tables_cta(p);
     return;
   }
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
-    const SlotIn si = load_slot(p, g);
+    // direct mode: the layout kernel is the launch just before, so its codes
+    // (and routed weights) are read only after the wait
+    SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
+    int gcode = -1;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -201,14 +401,19 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
           pdl_trigger();
           waited = true;
         }
-        resolve_rows(p, g, rows_s, si);
+        if (DIRECT) {  // the slot loads and (first token) the totals' loads in flight together
+          si = load_slot(p, g);
+          gcode = load_group_code(p, g);
+          if (!offsets_done) direct_offsets(p, dsm, false);
+          offsets_done = true;
+        }
+        resolve_token<DIRECT>(p, g, rows_s, si, gcode, dsm);
+        if (DIRECT && g + nb >= p.T) ticket = direct_count_out(p);
         __syncthreads();
       }
 #pragma unroll
       for (int i = 0; i < VPT; ++i) {
-        float m = amax8(val[i]);
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float m = block_amax8(val[i]);
         sc[i] = __fdiv_rn(m, 448.0f);
         code[i] = quant8(val[i], sc[i], m);
       }
@@ -229,6 +434,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
     }
     par ^= 1;  // token n+2 rewrites this buffer only after token n+1's barrier
   }
+  if (DIRECT) direct_end(p, ticket);
 }
 
 // FP8 with x 32-byte aligned: each thread takes 16 consecutive values (one
@@ -237,23 +443,29 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
 // instead of once per 8, and the quotients run two per instruction. Each
 // chunk is quantised and stored to the token's k rows (16-byte stores) before
 // the next, so only the loaded rows stay in registers.
-template <int CPT>
+template <int CPT, bool DIRECT>
 __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const DispatchArgs p) {
   // the k receive rows of the current token; two buffers, alternating per token
   __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  extern __shared__ int dsm[];  // tables CTAs and direct mode
   int par = 0;
   const int nch = p.H >> 4;  // 32-byte chunks (16 values) per row
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
-  bool waited = false;
+  bool waited = false, offsets_done = false;
+  unsigned ticket = 0u;
   if ((int)blockIdx.x < p.tab_ctas) {
-    tables_cta(p);
+    if (DIRECT) direct_tables_cta(p, dsm);
+    else tables_cta(p);
     return;
   }
   const long long nb = gridDim.x - p.tab_ctas;
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
-    const SlotIn si = load_slot(p, g);
+    // direct mode: the layout kernel is the launch just before, so its codes
+    // (and routed weights) are read only after the wait
+    SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
+    int gcode = -1;
     const uint16_t* src = p.x + g * p.H;
     for (int c0 = 0; c0 < nch; c0 += CPT * kDispatchThreads) {
       uint4 va[CPT], vb[CPT];
@@ -273,14 +485,19 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
           pdl_trigger();
           waited = true;
         }
-        resolve_rows(p, g, rows_s, si);
+        if (DIRECT) {  // the slot loads and (first token) the totals' loads in flight together
+          si = load_slot(p, g);
+          gcode = load_group_code(p, g);
+          if (!offsets_done) direct_offsets(p, dsm, false);
+          offsets_done = true;
+        }
+        resolve_token<DIRECT>(p, g, rows_s, si, gcode, dsm);
+        if (DIRECT && g + nb >= p.T) ticket = direct_count_out(p);
         __syncthreads();
       }
 #pragma unroll
       for (int i = 0; i < CPT; ++i) {
-        float m = fmaxf(amax8(va[i]), amax8(vb[i]));
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float m = block_amax16(va[i], vb[i]);
         const float sc = __fdiv_rn(m, 448.0f);
         const uint4 code = quant16(va[i], vb[i], sc, m);
         const int c = c0 + i * kDispatchThreads + tid;
@@ -296,6 +513,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
     }
     par ^= 1;  // token n+2 rewrites this buffer only after token n+1's barrier
   }
+  if (DIRECT) direct_end(p, ticket);
 }
 
 // k_dispatch_fp8w for CTAs that take several tokens: while a token is
@@ -358,9 +576,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 7) k_dispatch_fp8s(const Dis
         va = *reinterpret_cast<const uint4*>(row + 16 * c);
         vb = *reinterpret_cast<const uint4*>(row + 16 * c + 8);
       }
-      float m = fmaxf(amax8(va), amax8(vb));
-#pragma unroll
-      for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const float m = block_amax16(va, vb);
       const float sc = __fdiv_rn(m, 448.0f);
       const uint4 code = quant16(va, vb, sc, m);
       if (c < nch) {
@@ -374,6 +590,94 @@ __global__ void __launch_bounds__(kDispatchThreads, 7) k_dispatch_fp8s(const Dis
     }
   }
   cp_async_wait_all();  // no copy outlives the CTA
+}
+
+// k_dispatch_fp8s with the stores to the k receive rows done by the TMA
+// engine: each token's codes and scales are quantised into a shared-memory
+// row (two, alternating per token) and one thread issues one bulk copy per
+// receive row for the codes and one for the scales, so the copy no longer
+// spends an instruction per 16 bytes and receive row. Needs H a multiple of
+// 512 (16-byte scale rows) and 16-byte aligned receive buffers.
+// Dynamic shared memory: x rows [2][H] bf16 | codes [2][H] | scales [2][H/128].
+template <int CPT>
+__global__ void __launch_bounds__(kDispatchThreads, 5) k_dispatch_fp8b(const DispatchArgs p) {
+  extern __shared__ __align__(16) uint16_t xs[];  // [2][H]
+  __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  const int nch = p.H >> 4;
+  const int nblk = p.H >> 7;
+  const int tid = threadIdx.x;
+  if ((int)blockIdx.x < p.tab_ctas) {
+    tables_cta(p);
+    return;
+  }
+  uint8_t* qs = reinterpret_cast<uint8_t*>(xs + 2 * p.H);  // [2][H] codes
+  float* scs = reinterpret_cast<float*>(qs + 2 * p.H);     // [2][nblk] scales
+  const long long nb = gridDim.x - p.tab_ctas;
+  auto stage = [&](long long tok, int buf) {
+    if (tok < p.T) {
+      const uint16_t* src = p.x + tok * p.H;
+      uint16_t* dst = xs + buf * p.H;
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = i * kDispatchThreads + tid;
+        if (c < nch) {
+          cp_async16(dst + 16 * c, src + 16 * c);
+          cp_async16(dst + 16 * c + 8, src + 16 * c + 8);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  long long g = p.g0 + blockIdx.x - p.tab_ctas;
+  stage(g, 0);
+  bool waited = false;
+  int par = 0;
+  for (; g < p.T; g += nb, par ^= 1) {
+    const SlotIn si = load_slot(p, g);
+    stage(g + nb, par ^ 1);
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    int* rows_s = rows_buf[par];
+    resolve_rows(p, g, rows_s, si);
+    if (tid == 0) bulk_wait_read_prev();  // the copies of two tokens ago have read this buffer
+    __syncthreads();
+    cp_async_wait_prev();  // this token's chunks (this thread's own copies) have landed
+    const uint16_t* row = xs + par * p.H;
+    uint8_t* q = qs + par * p.H;
+    float* sq = scs + par * nblk;
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) {
+      const int c = i * kDispatchThreads + tid;
+      uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
+      if (c < nch) {
+        va = *reinterpret_cast<const uint4*>(row + 16 * c);
+        vb = *reinterpret_cast<const uint4*>(row + 16 * c + 8);
+      }
+      const float m = block_amax16(va, vb);
+      const float sc = __fdiv_rn(m, 448.0f);
+      const uint4 code = quant16(va, vb, sc, m);
+      if (c < nch) {
+        *reinterpret_cast<uint4*>(q + 16 * c) = code;
+        if ((tid & 7) == 0) sq[c >> 3] = sc;
+      }
+    }
+    fence_smem_to_async();
+    __syncthreads();
+    if (tid == 0) {
+      for (int j = 0; j < p.k; ++j) {
+        const int r = rows_s[j];
+        if (r < 0) continue;
+        bulk_store(static_cast<uint8_t*>(p.recv) + (long long)r * p.H, q, (uint32_t)p.H);
+        bulk_store(p.recv_scale + (long long)r * nblk, sq, (uint32_t)nblk * 4u);
+      }
+      bulk_commit();
+    }
+  }
+  cp_async_wait_all();  // no copy outlives the CTA
+  if (tid == 0) bulk_wait_all();
 }
 
 // AllGather comparator, stage 1: every token row (quantised once for FP8) is
@@ -395,9 +699,7 @@ __global__ void __launch_bounds__(kDispatchThreads) k_allgather(const AllGatherA
         const int v = v0 + i * kDispatchThreads + tid;
         val[i] = v < nvec ? ld_stream(src + v) : make_uint4(0u, 0u, 0u, 0u);
         if (FP8) {
-          float m = amax8(val[i]);
-#pragma unroll
-          for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          const float m = block_amax8(val[i]);
           sc[i] = __fdiv_rn(m, 448.0f);
           code[i] = quant8(val[i], sc[i], m);
         }
@@ -476,6 +778,27 @@ cudaError_t launch_allgather(const AllGatherArgs& a, bool fp8, int num_sms, cuda
   return launch_pdl(k_allgather_filter<false>, grid, block, 0, st, a);
 }
 
+template <bool DIRECT>
+cudaError_t launch_fp8w(const DispatchArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+  const int nch = a.H >> 4;
+  if (nch <= 128) return launch_pdl(k_dispatch_fp8w<1, DIRECT>, grid, block, smem, st, a);
+  if (nch <= 256) return launch_pdl(k_dispatch_fp8w<2, DIRECT>, grid, block, smem, st, a);
+  return launch_pdl(k_dispatch_fp8w<4, DIRECT>, grid, block, smem, st, a);
+}
+
+template <bool FP8, bool DIRECT>
+cudaError_t launch_vec(const DispatchArgs& a, dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+  const int nvec = a.H >> 3;
+  if (FP8) {
+    if (nvec <= 128) return launch_pdl(k_dispatch_fp8<1, DIRECT>, grid, block, smem, st, a);
+    if (nvec <= 512) return launch_pdl(k_dispatch_fp8<4, DIRECT>, grid, block, smem, st, a);
+    return launch_pdl(k_dispatch_fp8<8, DIRECT>, grid, block, smem, st, a);
+  }
+  if (nvec <= 128) return launch_pdl(k_dispatch_bf16<1, DIRECT>, grid, block, smem, st, a);
+  if (nvec <= 512) return launch_pdl(k_dispatch_bf16<4, DIRECT>, grid, block, smem, st, a);
+  return launch_pdl(k_dispatch_bf16<8, DIRECT>, grid, block, smem, st, a);
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaStream_t st) {
   long long blocks = a.T - a.g0 < 0 ? 0 : a.T - a.g0;
   const long long cap = (long long)num_sms * 16;  // 16 CTAs of 128 threads fill an SM
@@ -483,32 +806,39 @@ cudaError_t launch_dispatch(const DispatchArgs& a, bool fp8, int num_sms, cudaSt
   if (blocks == 0 && a.tab_ctas == 0) return cudaSuccess;
   if (blocks == 0) return launch_tables(a.tab, st);
   const dim3 grid((int)(blocks + a.tab_ctas)), block(kDispatchThreads);
-  const size_t smem = a.tab_ctas > 0 ? (size_t)(a.tab.E + 32) * sizeof(int) : 0;
-  const int nvec = a.H >> 3;
+  const size_t smem = a.direct ? (size_t)direct_smem_ints(a.E) * sizeof(int)
+                      : a.tab_ctas > 0 ? (size_t)(a.tab.E + 32) * sizeof(int) : 0;
   if (fp8 && (reinterpret_cast<uintptr_t>(a.x) & 31) == 0) {
     const int nch = a.H >> 4;
     // at least 16 tokens per CTA and two rows fit in shared memory: stage rows
-    // ahead (with fewer tokens per CTA the lost CTA per SM costs more)
+    // ahead (with fewer tokens per CTA the lost CTA per SM costs more); the
+    // direct mode (one token per CTA) never has that many
     const size_t stage_smem = (size_t)2 * a.H * sizeof(uint16_t);
-    if (a.T - a.g0 >= 16 * blocks && nch <= 4 * kDispatchThreads && stage_smem <= 48 * 1024) {
+    if (!a.direct && a.T - a.g0 >= 16 * blocks && nch <= 4 * kDispatchThreads &&
+        stage_smem <= 48 * 1024) {
+      // receive rows stored by bulk copies when the scale rows are 16-byte
+      // multiples (H a multiple of 512) and the buffers 16-byte aligned
+      const size_t bulk_smem = stage_smem + (size_t)2 * a.H + (size_t)2 * (a.H >> 7) * sizeof(float);
+      if ((a.H & 511) == 0 && (reinterpret_cast<uintptr_t>(a.recv_scale) & 15) == 0 &&
+          bulk_smem <= 48 * 1024 && a.send_pos == nullptr && a.slot_Tr == 0) {
+        const size_t sm = bulk_smem > smem ? bulk_smem : smem;
+        if (nch <= 128) return launch_pdl(k_dispatch_fp8b<1>, grid, block, sm, st, a);
+        else if (nch <= 256) return launch_pdl(k_dispatch_fp8b<2>, grid, block, sm, st, a);
+        else return launch_pdl(k_dispatch_fp8b<4>, grid, block, sm, st, a);
+      }
       const size_t sm = stage_smem > smem ? stage_smem : smem;
       if (nch <= 128) return launch_pdl(k_dispatch_fp8s<1>, grid, block, sm, st, a);
       else if (nch <= 256) return launch_pdl(k_dispatch_fp8s<2>, grid, block, sm, st, a);
       else return launch_pdl(k_dispatch_fp8s<4>, grid, block, sm, st, a);
     }
-    if (nch <= 128) return launch_pdl(k_dispatch_fp8w<1>, grid, block, smem, st, a);
-    else if (nch <= 256) return launch_pdl(k_dispatch_fp8w<2>, grid, block, smem, st, a);
-    else return launch_pdl(k_dispatch_fp8w<4>, grid, block, smem, st, a);
+    return a.direct ? launch_fp8w<true>(a, grid, block, smem, st)
+                    : launch_fp8w<false>(a, grid, block, smem, st);
   }
-  if (fp8) {  // x only 16-byte aligned
-    if (nvec <= 128) return launch_pdl(k_dispatch_fp8<1>, grid, block, smem, st, a);
-    else if (nvec <= 512) return launch_pdl(k_dispatch_fp8<4>, grid, block, smem, st, a);
-    else return launch_pdl(k_dispatch_fp8<8>, grid, block, smem, st, a);
-  } else {
-    if (nvec <= 128) return launch_pdl(k_dispatch_bf16<1>, grid, block, smem, st, a);
-    else if (nvec <= 512) return launch_pdl(k_dispatch_bf16<4>, grid, block, smem, st, a);
-    else return launch_pdl(k_dispatch_bf16<8>, grid, block, smem, st, a);
-  }
+  if (fp8)  // x only 16-byte aligned
+    return a.direct ? launch_vec<true, true>(a, grid, block, smem, st)
+                    : launch_vec<true, false>(a, grid, block, smem, st);
+  return a.direct ? launch_vec<false, true>(a, grid, block, smem, st)
+                  : launch_vec<false, false>(a, grid, block, smem, st);
 }
 
 cudaError_t launch_tables(const TablesArgs& t, cudaStream_t st) {

@@ -167,9 +167,7 @@ __device__ __forceinline__ bool fused_body(const FusedArgs& f, int* smem) {
       const int tl = on ? it / nvec : 0, v = on ? it - tl * nvec : 0;
       const uint4 val = on ? (f.prefetch_x ? xs[it] : ld_stream(gsrc + it)) : make_uint4(0u, 0u, 0u, 0u);
       if (FP8) {
-        float m = amax8(val);
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float m = block_amax8(val);
         const float sc = __fdiv_rn(m, 448.0f);
         const uint2 code = quant8(val, sc, m);
         if (on) {

@@ -64,6 +64,10 @@ struct LayoutArgs {
   // reader and clears the totals after reading them, ready for the next
   // layout: no host-side state, so a captured graph replays correctly.
   int32_t* acc_add;
+  // Per-(source, expert) totals [P][E] accumulated the same way, or null: with
+  // them (and acc_add) the dispatch can lay itself out without the scan
+  // kernel (DispatchArgs::direct).
+  int32_t* acc_se;
 };
 
 // Per-source tables of the layout, one source rank s per CTA (source_tables):
@@ -113,6 +117,24 @@ struct DispatchArgs {
   int slot_Tr, P;
   uint32_t* status;       // MOE_STATUS_SLOT_OVERFLOW (fixed slots), MOE_STATUS_BOUNDS
   long long row_limit;    // rows of the destination buffer (debug bounds checks)
+  // Direct mode (small layouts, no scan kernel after the layout): the expert
+  // offsets come from the per-expert totals acc and a slot's place inside its
+  // expert from the per-(source, expert) totals acc_se of earlier sources plus
+  // the raw chunk counts in hist of its own source's earlier chunks. CTA 0
+  // writes the per-expert arrays; every CTA counts itself out on `arrive`
+  // after reading the totals and the last one clears them and the counter.
+  // direct_G: lanes that sum one slot's earlier counts (a power of two <= 32,
+  // direct_G * k <= the CTA's threads).
+  int direct, direct_G;
+  int32_t* acc;           // [E]
+  int32_t* acc_se;        // [P][E]
+  unsigned* arrive;
+  int32_t* n_raw;         // [E]  (written by CTA 0)
+  int32_t* n_kept;        // [E]
+  int32_t* expert_offset_out;  // [E+1]
+  int32_t* rank_base;     // [P+1]
+  int32_t* totals;        // [4]
+  long long Na;
 };
 
 // Persistent single-launch route/layout/dispatch (fused.cu).
@@ -225,7 +247,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Launchers (return cudaGetLastError() of the launch).
-cudaError_t launch_layout(const LayoutArgs& a, bool route, int num_sms, cudaStream_t st);
+// The layout kernel, then (scan = true) the scan kernel.
+cudaError_t launch_layout(const LayoutArgs& a, bool route, int num_sms, cudaStream_t st,
+                          bool scan = true);
+// The scan kernel alone, for a layout launched with scan = false.
+cudaError_t launch_scan(const LayoutArgs& a, cudaStream_t st);
 cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long long T,
                               int E, int k, int num_sms, cudaStream_t st);
 size_t layout_smem_bytes(int E, int tpc, int k, int P);
@@ -268,7 +294,13 @@ struct moe_handle {
   unsigned long long layout_gen, dispatch_gen;
   int tables_pending;       // per-source tables of the last layout not yet built
   int32_t* acc;             // [E] per-expert totals (zero between layouts)
+  int32_t* acc_se;          // [P*E] per-(source, expert) totals (zero between layouts)
   int acc_dirty;            // a failed layout launch may have left partial sums
+  // 0: the last layout is scanned (or none ran); 1: laid out for the direct
+  // dispatch, not scanned, totals in acc/acc_se; 2: a direct dispatch ran on
+  // it (totals consumed and cleared, chunk counts still unscanned)
+  int scan_state;
+  int direct_ok;            // small enough for the direct dispatch
   int fixed_rows;           // the last dispatch wrote fixed per-(source, expert) slots
   long long wait_limit;     // bounded device waits (persistent path)
 };

@@ -84,6 +84,10 @@ __device__ void offsets_from_totals(const LayoutArgs& p, int* smem) {
   }
   if (dr) atomicAdd(&red[0], dr);
   if (rw) atomicAdd(&red[1], rw);
+  // per-(source, expert) totals of a layout laid out for the direct dispatch
+  // are not needed here: clear them too for the next layout
+  if (p.acc_se)
+    for (int i = tid; i < p.P * E; i += NT) p.acc_se[i] = 0;
   const int total = cta_exclusive_scan(sk, E, tmp);
   for (int e = tid; e <= E; e += NT) p.expert_offset[e] = e < E ? sk[e] : total;
   for (int d = tid; d <= p.P; d += NT) p.rank_base[d] = d < p.P ? sk[d * p.L] : total;
@@ -289,16 +293,21 @@ cudaError_t layout_prepare_all(size_t* layout_dyn_max, size_t* scan_dyn_max) {
   return cudaSuccess;
 }
 
-cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cudaStream_t st) {
+cudaError_t launch_scan(const LayoutArgs& a, cudaStream_t st) {
+  const int scan_blocks = (a.E + kScanThreads / 32 - 1) / (kScanThreads / 32) + (a.acc_add ? 1 : 0);
+  return launch_pdl(k_scan, dim3(scan_blocks), dim3(kScanThreads), scan_smem_bytes(a.E, a.P), st,
+                    a);
+}
+
+cudaError_t launch_layout(const LayoutArgs& a, bool route, int /*num_sms*/, cudaStream_t st,
+                          bool scan) {
   const size_t smem = layout_smem_bytes(a.E, a.tpc, a.k, a.P);
   const int epl = experts_per_lane(a.E);
   void* fn = route ? layout_kernel_ptr<true>(epl) : layout_kernel_ptr<false>(epl);
   cudaError_t err = launch_pdl(reinterpret_cast<void (*)(const LayoutArgs)>(fn), dim3(a.nchunks),
                                dim3(kLayoutThreads), smem, st, a);
-  if (err != cudaSuccess) return err;
-  const int scan_blocks = (a.E + kScanThreads / 32 - 1) / (kScanThreads / 32) + (a.acc_add ? 1 : 0);
-  return launch_pdl(k_scan, dim3(scan_blocks), dim3(kScanThreads), scan_smem_bytes(a.E, a.P), st,
-                    a);
+  if (err != cudaSuccess || !scan) return err;
+  return launch_scan(a, st);
 }
 
 cudaError_t launch_route_only(const float* logits, int32_t* ids, float* w, long long T, int E,

@@ -80,6 +80,49 @@ __device__ __forceinline__ void topk_select(unsigned (&key)[EPL], int k, int lan
   }
 }
 
+// topk_select for NT tokens at once, round by round: the NT tokens' local
+// scans and warp reductions are independent, so their latencies overlap
+// (NT-way instruction-level parallelism). Tokens u >= nu hold zero keys
+// (every lane's best is then no expert) and their outputs are unused.
+template <int EPL, int NT>
+__device__ __forceinline__ void topk_select_multi(unsigned (&key)[NT][EPL], int k, int lane,
+                                                  int (&out_id)[NT], float (&out_z)[NT]) {
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+    out_id[u] = -1;
+    out_z[u] = 0.0f;
+  }
+  for (int j = 0; j < k; ++j) {
+    unsigned bk[NT], bi[NT], mx[NT], wn[NT];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+      bk[u] = 0u;
+      bi[u] = 0xffffffffu;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        if (key[u][i] > bk[u]) {  // strict: the lowest register (expert) wins a tie in a lane
+          bk[u] = key[u][i];
+          bi[u] = (unsigned)(i * 32 + lane);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NT; ++u) mx[u] = __reduce_max_sync(kFull, bk[u]);
+#pragma unroll
+    for (int u = 0; u < NT; ++u) wn[u] = __reduce_min_sync(kFull, bk[u] == mx[u] ? bi[u] : 0xffffffffu);
+#pragma unroll
+    for (int u = 0; u < NT; ++u) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (wn[u] == (unsigned)(i * 32 + lane)) key[u][i] = 0u;
+      if (lane == j) {
+        out_id[u] = (int)wn[u];
+        out_z[u] = key_value(mx[u]);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float pow2f(int n) {  // 2^n for -126 <= n <= 127
   return __uint_as_float((unsigned)(n + 127) << 23);
 }
@@ -100,24 +143,49 @@ __device__ __forceinline__ void route_group_warp(const float* __restrict__ logit
   valid = grp < ntok && slot < k;
   id = -1;
   float my_z = 0.0f;
-  // The logits of up to kPre tokens are loaded before any is selected.
-  constexpr int kPre = EPL >= 32 ? 1 : (32 / EPL < 4 ? 32 / EPL : 4);
-  for (int t0 = 0; t0 < ntok; t0 += kPre) {
-    unsigned key[kPre][EPL];
+  // The logits of up to kPre tokens are loaded before any is selected, and
+  // their selections run interleaved; one token alone takes the plain path.
+  // (two at E <= 512 beyond 256 experts per warp's registers, so that the
+  // interleaved keys still fit the kernel's register budget without spills)
+  constexpr int kPre = EPL >= 32 ? 1 : EPL >= 8 ? 2 : 4;
+  if (ntok == 1 || kPre == 1) {
+    for (int t0 = 0; t0 < ntok; ++t0) {
+      unsigned key[EPL];
+      load_keys<EPL>(logits + (g0 + t0) * (long long)E, E, lane, key);
+      int tid_;
+      float tz;
+      topk_select<EPL>(key, k, lane, tid_, tz);
+      const int sid = __shfl_sync(kFull, tid_, slot);
+      const float sz = __shfl_sync(kFull, tz, slot);
+      if (grp == t0) {
+        id = sid;
+        my_z = sz;
+      }
+    }
+  } else {
+    for (int t0 = 0; t0 < ntok; t0 += kPre) {
+      unsigned key[kPre][EPL];
 #pragma unroll
-    for (int u = 0; u < kPre; ++u)
-      if (t0 + u < ntok) load_keys<EPL>(logits + (g0 + t0 + u) * (long long)E, E, lane, key[u]);
+      for (int u = 0; u < kPre; ++u) {
+        if (t0 + u < ntok) {
+          load_keys<EPL>(logits + (g0 + t0 + u) * (long long)E, E, lane, key[u]);
+        } else {
 #pragma unroll
-    for (int u = 0; u < kPre; ++u) {
-      if (t0 + u < ntok) {
-        int tid_;
-        float tz;
-        topk_select<EPL>(key[u], k, lane, tid_, tz);
-        const int sid = __shfl_sync(kFull, tid_, slot);
-        const float sz = __shfl_sync(kFull, tz, slot);
-        if (grp == t0 + u) {
-          id = sid;
-          my_z = sz;
+          for (int i = 0; i < EPL; ++i) key[u][i] = 0u;
+        }
+      }
+      int tid_[kPre];
+      float tz[kPre];
+      topk_select_multi<EPL, kPre>(key, k, lane, tid_, tz);
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        if (t0 + u < ntok) {
+          const int sid = __shfl_sync(kFull, tid_[u], slot);
+          const float sz = __shfl_sync(kFull, tz[u], slot);
+          if (grp == t0 + u) {
+            id = sid;
+            my_z = sz;
+          }
         }
       }
     }
@@ -262,7 +330,6 @@ __device__ __forceinline__ void layout_chunk(const LayoutArgs& p, int b, int* sm
 
   for (int i = tid; i < wcnt_ints; i += kLayoutThreads) wcnt[i] = 0;
   pdl_wait();  // logits / ids may come from the previous kernel
-  pdl_trigger();
 
   if (ROUTE) {
     int K2 = 1;
@@ -317,6 +384,7 @@ __device__ __forceinline__ void layout_chunk(const LayoutArgs& p, int b, int* sm
     }
     p.hist[(long long)e * p.nchunks + b] = run;  // transposed: [E][nchunks]
     if (p.acc_add && run) atomicAdd(p.acc_add + e, run);  // the expert's total
+    if (p.acc_se && run) atomicAdd(p.acc_se + (long long)s * E + e, run);  // its source's
   }
   __syncthreads();
   // Pass 2: stable rank of every assignment within the chunk and expert.
@@ -332,7 +400,10 @@ __device__ __forceinline__ void layout_chunk(const LayoutArgs& p, int b, int* sm
     __syncwarp();
     if (i < end) p.acode[a0 + i] = code;
   }
-
+  // The next kernel may launch only now: a dispatch that follows directly
+  // (no scan kernel) would otherwise start loading its token rows while the
+  // chunks still route, competing with them for the memory system.
+  pdl_trigger();
 }
 
 }  // namespace

@@ -115,6 +115,11 @@ typedef struct moe_handle *moe_handle_t;
  * array is complete, in stream order:
  *   - expert_count, expert_count_raw, expert_offset, rank_base, totals: after
  *     the layout call (moe_dispatch_layout, moe_route_dispatch_layout);
+ *     except for small layers (at most 32 ranks and T at most 16 times the
+ *     SM count, e.g. decode), whose layout call only counts and whose
+ *     following moe_dispatch lays itself out from the counts ("direct
+ *     dispatch", one launch boundary less): there these are complete after
+ *     that dispatch, or after moe_layout_tables;
  *   - src_expert_count, src_expert_kept, count_matrix, send_offset,
  *     recv_offset (the per-source tables): after the dispatch that follows the
  *     layout. The copy does not need them, so moe_dispatch and

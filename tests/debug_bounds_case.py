@@ -52,6 +52,10 @@ def corrupt():
     w = torch.from_numpy(inp.w).cuda()
     bad_e = 5
     layer.layout(ids)
+    # the layout tables first: the layout is then scanned, and the dispatch
+    # reads the expert offsets from the workspace (a small layout would
+    # otherwise be dispatched directly from the per-expert totals)
+    layer.layout_tables()
     view = layer.layout_view()
     view["expert_offset"][bad_e] = layer.rows + 5  # past the receive buffer
     layer.dispatch(x, w)
@@ -66,7 +70,7 @@ def corrupt():
     assert (inv[flat == bad_e] == -1).all()
     ok = flat != bad_e
     assert np.array_equal(inv[ok], lay["inv"][ok])
-    # a clean layer afterwards on the same handle is exact again
+    # a clean layer afterwards on the same handle (direct dispatch) is exact again
     layer.layout(ids)
     layer.dispatch(x, w)
     torch.cuda.synchronize()

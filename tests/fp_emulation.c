@@ -3,9 +3,9 @@
  * floating-point procedures the CUDA kernels use, so that the claims made
  * about them can be checked on the host:
  *
- *   1. the FP8 quantiser's quotient x / s by Markstein's FMA correction with a
- *      float-float reciprocal of s (payload_device.cuh, div_by_scale), against
- *      the IEEE quotient RN(x / s);
+ *   1. the FP8 quantiser's quotient x / s by one Markstein FMA correction of
+ *      x * RN(1/s) (payload_device.cuh, quant_words), against the IEEE
+ *      quotient RN(x / s);
  *   2. the router's softmax weights in float-float arithmetic (ffmath.cuh and
  *      route_group_warp in layout_device.cuh), against the same softmax
  *      evaluated in double and rounded once to fp32.
@@ -58,15 +58,15 @@ float emu_fmaf(float a, float b, float c) {
 /* 1. Markstein quotient                                                   */
 /* ---------------------------------------------------------------------- */
 
-/* The kernel's steps for one value: yh = RN(1/s), yl = RN(RN(1 - s*yh) * yh),
- * q0 = RN(x*yh + x*yl), r = RN(x - s*q0), q = RN(r*yh + q0), sign of x kept. */
+/* The kernel's steps for one value: y = RN(1/s), q0 = RN(x*y),
+ * r = RN(x - s*q0), q = RN(r*y + q0) (Markstein's single correction). The
+ * kernel then takes the sign of the e4m3 code from x itself, so the sign of
+ * a zero quotient returned here does not matter. */
 float emu_div_by_scale(float x, float s) {
-    const float yh = 1.0f / s;
-    const float yl = emu_fmaf(-s, yh, 1.0f) * yh;
-    const float q0 = emu_fmaf(x, yh, x * yl);
+    const float y = 1.0f / s;
+    const float q0 = x * y;
     const float r = emu_fmaf(-s, q0, x);
-    const float q = emu_fmaf(r, yh, q0);
-    return f_of(u_of(q) | (u_of(x) & 0x80000000u));
+    return emu_fmaf(r, y, q0);
 }
 
 /* Every positive finite bf16 amax with encoding in [amax_lo, amax_hi) and

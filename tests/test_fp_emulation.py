@@ -1,12 +1,13 @@
 """CPU checks of two floating-point procedures of the CUDA kernels, emulated
 operation for operation in tests/fp_emulation.c (no GPU needed):
 
-* the FP8 quantiser divides by the block scale with Markstein's FMA-corrected
-  quotient instead of an IEEE division; swept over every bf16 amax >= 2^-64
-  and every bf16 |x| <= amax, its quotient must equal RN(x / s) except where
-  both are so small that the e4m3 code is a signed zero (the codes, which the
-  pages fix -- "[Infra-10] All-to-All Optimization", 4.1, FP8 on the wire;
-  pplx blog, "Dispatch", block scale factors -- are then identical);
+* the FP8 quantiser divides by the block scale with one Markstein FMA
+  correction of x * RN(1/s) instead of an IEEE division, and takes each
+  code's sign from x; swept over every bf16 amax >= 2^-64 and every bf16
+  |x| <= amax, its quotient must equal RN(x / s) except where both are so
+  small that the e4m3 code is a signed zero (the codes, which the pages fix
+  -- "[Infra-10] All-to-All Optimization", 4.1, FP8 on the wire; pplx blog,
+  "Dispatch", block scale factors -- are then identical);
 * the router's softmax weights are evaluated in float-float arithmetic; on
   millions of top-8 weights they must be within one fp32 ulp of the oracle's
   double softmax rounded to fp32, and the float-float exp itself must carry
@@ -129,8 +130,14 @@ def test_markstein_quotient_sampled_with_signs(emu):
         v = np.clip(v, -448, 448)
         return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
 
-    assert np.array_equal(codes(q), codes(ref))
-    same = q.view(np.uint32) == ref.view(np.uint32)
+    # the kernel's code: the quotient's e4m3 magnitude, the sign of x
+    x[:1000] = np.float32(-0.0)  # negative zeros, whose quotient may lose the sign
+    q = np.empty(n, np.float32)
+    emu.markstein_many(n, x, s, q)
+    ref = (x / s).astype(np.float32)
+    kernel = (codes(np.abs(q)) | (np.signbit(x).astype(np.uint8) << 7)).astype(np.uint8)
+    assert np.array_equal(kernel, codes(ref))
+    same = np.abs(q).view(np.uint32) == np.abs(ref).view(np.uint32)
     assert np.all(same | (np.abs(ref) < 2.0 ** -40))
 
 

@@ -161,13 +161,18 @@ def test_fp8_capacity_parity(gpu, cap):
     _check(wl, inp)
 
 
-def test_fp8_dispatch_many_tokens_per_cta(gpu):
+@pytest.mark.parametrize("H,cap", [(256, 0), (512, 0), (1536, 1200)])
+def test_fp8_dispatch_many_tokens_per_cta(gpu, H, cap):
     """More than 16 tokens per dispatch CTA (T = 40000 over at most 16 CTAs
     per SM): the FP8 dispatch stages each CTA's next row in shared memory
-    while storing the current one. Every element against the oracle."""
-    wl = W.UNIFORM_FP8.scaled("fp8_staged", Tr=5000, H=256)
+    while storing the current one; with H a multiple of 512 the receive rows
+    are stored by bulk copies from shared memory (one with capacity drops).
+    Every element against the oracle."""
+    wl = W.UNIFORM_FP8.scaled(f"fp8_staged_{H}", Tr=5000, H=H, cap=cap)
     inp = W.make_inputs(wl)
-    compare(wl, run_gpu(wl, inp), run_oracle(wl, inp), routed=False)
+    st = compare(wl, run_gpu(wl, inp), run_oracle(wl, inp), routed=False)
+    if cap:
+        assert st["kept"] < wl.Na
 
 
 @pytest.mark.parametrize("name", ["uniform_fp8", "prefill_cap"])
@@ -190,6 +195,11 @@ def test_fp8_extreme_values(gpu):
     vals = np.float32(rng.standard_normal((wl.T, wl.H))) * \
         np.float32(10.0) ** rng.integers(-30, 30, (wl.T, 1)).astype(np.float32)
     vals[:, :128] *= np.float32(1e-6) * (np.arange(128) % 2 == 0)  # wide dynamic range
+    # blocks of subnormal values (bf16 keeps fp32's exponent range)
+    vals[0, 128:256] = rng.standard_normal(128).astype(np.float32) * np.float32(1e-39)
+    vals[1, 256:384] = np.float32(rng.integers(-3, 4, 128)) * np.float32(2.0 ** -133)
+    vals[2, 384:512] = -0.0  # an all-zero block of negative zeros
+    vals[3, 384:512] = np.where(np.arange(128) % 3 == 0, np.float32(-0.0), np.float32(1.5))
     inp.x[:] = W._bf16_bits_from_f32(vals.astype(np.float32))
     _check(wl, inp)
 

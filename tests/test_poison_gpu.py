@@ -55,11 +55,22 @@ def _check_rows(name, arr, written_rows):
     assert _all_ff(arr[~written_rows]), f"{name}: a row outside the kept rows was written"
 
 
+def _fp8_many_tokens_with_drops():
+    """Over 16 tokens per dispatch CTA and H a multiple of 512: the receive
+    rows are stored by bulk copies from shared memory."""
+    wl = W.UNIFORM_FP8.scaled("poison_bulk", Tr=5000, H=512, cap=1200)
+    return wl, W.make_inputs(wl)
+
+
+CASES = {"bf16_given_ids": _bf16_given_ids, "fp8_routed_drops": _fp8_routed_with_drops,
+         "fp8_bulk_drops": _fp8_many_tokens_with_drops}
+
+
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("case", ["bf16_given_ids", "fp8_routed_drops"])
+@pytest.mark.parametrize("case", list(CASES))
 def test_poisoned_buffers(gpu, mode, case):
     from combine_top_histogram_gb300 import MoeLayer
-    wl, inp = _bf16_given_ids() if case == "bf16_given_ids" else _fp8_routed_with_drops()
+    wl, inp = CASES[case]()
     layer = MoeLayer(wl.P, wl.Tr, wl.E, wl.k, wl.H, wl.dispatch_dtype, wl.cap, "cuda:0")
     flags = dict(two_stage=mode == "two_stage", fused=mode == "fused",
                  allgather=mode == "allgather", pipelined=3 if mode == "pipelined" else 0)
@@ -70,7 +81,7 @@ def test_poisoned_buffers(gpu, mode, case):
     st = compare(wl, g, o, routed=inp.logits is not None)
     assert g["status"] == 0
     n = st["kept"]
-    if case == "fp8_routed_drops":
+    if case in ("fp8_routed_drops", "fp8_bulk_drops"):
         assert o["layout"]["totals"][1] > 0  # the capacity dropped rows
     if case == "bf16_given_ids":
         assert o["layout"]["totals"][2] > 0  # some slots were masked
