@@ -594,18 +594,27 @@ __global__ void __launch_bounds__(kDispatchThreads, 7) k_dispatch_fp8s(const Dis
 
 // k_dispatch_fp8s with the stores to the k receive rows done by the TMA
 // engine: each token's codes and scales are quantised into a shared-memory
-// row (two, alternating per token) and one thread issues one bulk copy per
-// receive row for the codes and one for the scales, so the copy no longer
-// spends an instruction per 16 bytes and receive row. Needs H a multiple of
-// 512 (16-byte scale rows) and 16-byte aligned receive buffers.
+// row (two, alternating per token) and one thread of the last warp (the
+// issuer) copies them to the token's receive rows with one bulk copy per row
+// for the codes and one for the scales. The copy then no longer spends a store
+// instruction per 16 bytes and receive row. The stores of token n are issued
+// right after the barrier of token n+1, which is also the point where every
+// warp has written token n's row, so one barrier per token suffices; before
+// that barrier the issuer waits (a hardware wait) until its copies of token
+// n-1, the last ones reading the row buffer token n+1 will write, have read
+// it. Three receive-row lists rotate, since token n's list is read while
+// token n+2's is resolved. Each thread stages (cp.async) and reads the same
+// x chunks, so staging the next token's row needs no barrier. Needs H a
+// multiple of 512 (16-byte scale rows) and 16-byte aligned receive buffers.
 // Dynamic shared memory: x rows [2][H] bf16 | codes [2][H] | scales [2][H/128].
 template <int CPT>
 __global__ void __launch_bounds__(kDispatchThreads, 5) k_dispatch_fp8b(const DispatchArgs p) {
   extern __shared__ __align__(16) uint16_t xs[];  // [2][H]
-  __shared__ int rows_buf[2][MOE_MAX_TOPK];
+  __shared__ int rows_buf[3][MOE_MAX_TOPK];
   const int nch = p.H >> 4;
   const int nblk = p.H >> 7;
   const int tid = threadIdx.x;
+  const bool issuer = tid == kDispatchThreads - 32;  // lane 0 of the last warp
   if ((int)blockIdx.x < p.tab_ctas) {
     tables_cta(p);
     return;
@@ -628,11 +637,24 @@ __global__ void __launch_bounds__(kDispatchThreads, 5) k_dispatch_fp8b(const Dis
     }
     cp_async_commit();
   };
+  // the issuer's bulk copies of one token (its codes and scales in buffer b)
+  auto store_token = [&](const int* rows, int b) {
+    const uint8_t* q = qs + b * p.H;
+    const float* sq = scs + b * nblk;
+    for (int j = 0; j < p.k; ++j) {
+      const int r = rows[j];
+      if (r < 0) continue;
+      bulk_store(static_cast<uint8_t*>(p.recv) + (long long)r * p.H, q, (uint32_t)p.H);
+      bulk_store(p.recv_scale + (long long)r * nblk, sq, (uint32_t)nblk * 4u);
+    }
+    bulk_commit();
+  };
   long long g = p.g0 + blockIdx.x - p.tab_ctas;
   stage(g, 0);
   bool waited = false;
-  int par = 0;
-  for (; g < p.T; g += nb, par ^= 1) {
+  int n = 0;  // tokens of this CTA so far
+  for (; g < p.T; g += nb, ++n) {
+    const int par = n & 1;
     const SlotIn si = load_slot(p, g);
     stage(g + nb, par ^ 1);
     if (!waited) {
@@ -640,10 +662,12 @@ __global__ void __launch_bounds__(kDispatchThreads, 5) k_dispatch_fp8b(const Dis
       pdl_trigger();
       waited = true;
     }
-    int* rows_s = rows_buf[par];
+    int* rows_s = rows_buf[n % 3];
     resolve_rows(p, g, rows_s, si);
-    if (tid == 0) bulk_wait_read_prev();  // the copies of two tokens ago have read this buffer
+    if (issuer) bulk_wait_read_all();  // token n-2's copies have read buffer par
     __syncthreads();
+    // every warp has written token n-1's row (and its fence): store it
+    if (issuer && n > 0) store_token(rows_buf[(n + 2) % 3], par ^ 1);
     cp_async_wait_prev();  // this token's chunks (this thread's own copies) have landed
     const uint16_t* row = xs + par * p.H;
     uint8_t* q = qs + par * p.H;
@@ -665,19 +689,13 @@ __global__ void __launch_bounds__(kDispatchThreads, 5) k_dispatch_fp8b(const Dis
       }
     }
     fence_smem_to_async();
-    __syncthreads();
-    if (tid == 0) {
-      for (int j = 0; j < p.k; ++j) {
-        const int r = rows_s[j];
-        if (r < 0) continue;
-        bulk_store(static_cast<uint8_t*>(p.recv) + (long long)r * p.H, q, (uint32_t)p.H);
-        bulk_store(p.recv_scale + (long long)r * nblk, sq, (uint32_t)nblk * 4u);
-      }
-      bulk_commit();
-    }
+  }
+  __syncthreads();
+  if (issuer) {
+    if (n > 0) store_token(rows_buf[(n + 2) % 3], (n - 1) & 1);  // the last token
+    bulk_wait_all();
   }
   cp_async_wait_all();  // no copy outlives the CTA
-  if (tid == 0) bulk_wait_all();
 }
 
 // AllGather comparator, stage 1: every token row (quantised once for FP8) is

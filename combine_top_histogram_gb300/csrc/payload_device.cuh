@@ -140,10 +140,9 @@ __device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src,
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-// Waits until at most one committed group of this thread still reads its
-// shared-memory source.
-__device__ __forceinline__ void bulk_wait_read_prev() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// Waits until every committed group of this thread has read its source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Waits until every committed group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
