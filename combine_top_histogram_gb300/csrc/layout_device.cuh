@@ -123,6 +123,75 @@ __device__ __forceinline__ void topk_select_multi(unsigned (&key)[NT][EPL], int 
   }
 }
 
+// Top-k of one token by one warp through a threshold: tau, the k-th largest
+// of the 32 lane maxima (ties counted), is at most the token's k-th largest
+// key, since the lanes whose maximum is at least tau hold k such keys. So
+// every key of the top k is a candidate key >= tau (for N(0,1) logits, E =
+// 256 and k = 8, about a dozen). The candidates are compacted, one per lane,
+// through the warp's 32 (key, expert) pairs in cand, and k rounds of the
+// warp arg-max (larger key first, lower expert on ties) select them in
+// order, so the result is exactly topk_select's. Returns false, with the
+// outputs unset, when more than 32 keys are candidates or fewer than k keys
+// are non-zero; the caller then runs topk_select. key is left unchanged.
+// Lanes hold expert i*32 + lane in register i, as in topk_select.
+template <int EPL>
+__device__ __forceinline__ bool topk_threshold(const unsigned (&key)[EPL], int k, int lane,
+                                               uint2* cand, int& out_id, float& out_z) {
+  unsigned rest = key[0];
+#pragma unroll
+  for (int i = 1; i < EPL; ++i) rest = max(rest, key[i]);
+  unsigned tau = 0u;
+  int cnt = 0;
+  for (int r = 0; r < k; ++r) {  // warp-uniform
+    const unsigned m = __reduce_max_sync(kFull, rest);
+    if (m == 0u) break;
+    cnt += __popc(__ballot_sync(kFull, rest == m));
+    if (rest == m) rest = 0u;
+    if (cnt >= k) {
+      tau = m;
+      break;
+    }
+  }
+  if (tau == 0u) return false;
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) n += key[i] >= tau ? 1 : 0;
+  // this lane's first slot in cand: the candidates of the lanes below it
+  constexpr int kBits = EPL >= 32 ? 6 : EPL >= 16 ? 5 : EPL >= 8 ? 4 : EPL >= 4 ? 3 : 2;
+  const unsigned below = (1u << lane) - 1u;
+  int pos = 0, total = 0;
+#pragma unroll
+  for (int b = 0; b < kBits; ++b) {
+    const unsigned bal = __ballot_sync(kFull, (n >> b) & 1);
+    pos += __popc(bal & below) << b;
+    total += __popc(bal) << b;
+  }
+  if (total > 32) return false;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    if (key[i] >= tau) {
+      cand[pos] = make_uint2(key[i], (unsigned)(i * 32 + lane));
+      ++pos;
+    }
+  }
+  __syncwarp();
+  const uint2 c = lane < total ? cand[lane] : make_uint2(0u, 0xffffffffu);
+  __syncwarp();  // cand is free for the warp's next token
+  unsigned ck = c.x;
+  out_id = -1;
+  out_z = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const unsigned m = __reduce_max_sync(kFull, ck);
+    const unsigned win = __reduce_min_sync(kFull, ck == m ? c.y : 0xffffffffu);
+    if (c.y == win) ck = 0u;
+    if (lane == j) {
+      out_id = (int)win;
+      out_z = key_value(m);
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ float pow2f(int n) {  // 2^n for -126 <= n <= 127
   return __uint_as_float((unsigned)(n + 127) << 23);
 }
@@ -148,43 +217,69 @@ __device__ __forceinline__ void route_group_warp(const float* __restrict__ logit
   // (two at E <= 512 beyond 256 experts per warp's registers, so that the
   // interleaved keys still fit the kernel's register budget without spills)
   constexpr int kPre = EPL >= 32 ? 1 : EPL >= 8 ? 2 : 4;
-  if (ntok == 1 || kPre == 1) {
-    for (int t0 = 0; t0 < ntok; ++t0) {
-      unsigned key[EPL];
-      load_keys<EPL>(logits + (g0 + t0) * (long long)E, E, lane, key);
-      int tid_;
-      float tz;
-      topk_select<EPL>(key, k, lane, tid_, tz);
-      const int sid = __shfl_sync(kFull, tid_, slot);
-      const float sz = __shfl_sync(kFull, tz, slot);
-      if (grp == t0) {
-        id = sid;
-        my_z = sz;
-      }
-    }
-  } else {
-    for (int t0 = 0; t0 < ntok; t0 += kPre) {
-      unsigned key[kPre][EPL];
-#pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        if (t0 + u < ntok) {
-          load_keys<EPL>(logits + (g0 + t0 + u) * (long long)E, E, lane, key[u]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < EPL; ++i) key[u][i] = 0u;
+  bool done = false;
+  if constexpr (EPL >= 4) {
+    if (k <= 8) {
+      // the threshold top-k (topk_threshold), one token at a time; each warp
+      // of the block (at most kLayoutWarps) owns 32 pairs of cand_s
+      __shared__ uint2 cand_s[kLayoutWarps][32];
+      uint2* cand = cand_s[threadIdx.x >> 5];
+      for (int t0 = 0; t0 < ntok; ++t0) {
+        unsigned key[EPL];
+        load_keys<EPL>(logits + (g0 + t0) * (long long)E, E, lane, key);
+        int tid_;
+        float tz;
+        if (!topk_threshold<EPL>(key, k, lane, cand, tid_, tz))
+          topk_select<EPL>(key, k, lane, tid_, tz);
+        const int sid = __shfl_sync(kFull, tid_, slot);
+        const float sz = __shfl_sync(kFull, tz, slot);
+        if (grp == t0) {
+          id = sid;
+          my_z = sz;
         }
       }
-      int tid_[kPre];
-      float tz[kPre];
-      topk_select_multi<EPL, kPre>(key, k, lane, tid_, tz);
+      done = true;
+    }
+  }
+  if (!done) {
+    if (ntok == 1 || kPre == 1) {
+      for (int t0 = 0; t0 < ntok; ++t0) {
+        unsigned key[EPL];
+        load_keys<EPL>(logits + (g0 + t0) * (long long)E, E, lane, key);
+        int tid_;
+        float tz;
+        topk_select<EPL>(key, k, lane, tid_, tz);
+        const int sid = __shfl_sync(kFull, tid_, slot);
+        const float sz = __shfl_sync(kFull, tz, slot);
+        if (grp == t0) {
+          id = sid;
+          my_z = sz;
+        }
+      }
+    } else {
+      for (int t0 = 0; t0 < ntok; t0 += kPre) {
+        unsigned key[kPre][EPL];
 #pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        if (t0 + u < ntok) {
-          const int sid = __shfl_sync(kFull, tid_[u], slot);
-          const float sz = __shfl_sync(kFull, tz[u], slot);
-          if (grp == t0 + u) {
-            id = sid;
-            my_z = sz;
+        for (int u = 0; u < kPre; ++u) {
+          if (t0 + u < ntok) {
+            load_keys<EPL>(logits + (g0 + t0 + u) * (long long)E, E, lane, key[u]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) key[u][i] = 0u;
+          }
+        }
+        int tid_[kPre];
+        float tz[kPre];
+        topk_select_multi<EPL, kPre>(key, k, lane, tid_, tz);
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+          if (t0 + u < ntok) {
+            const int sid = __shfl_sync(kFull, tid_[u], slot);
+            const float sz = __shfl_sync(kFull, tz[u], slot);
+            if (grp == t0 + u) {
+              id = sid;
+              my_z = sz;
+            }
           }
         }
       }
