@@ -74,8 +74,29 @@ Plan make_plan(const moe_config_t* c, int num_sms) {
   if (tr < 1) tr = 1;
   if (tr > max_tpc) tr = max_tpc;
   if (tr > Tr) tr = Tr;
+  // More chunks than the GPU holds at once (two CTAs per SM, one from 512
+  // experts up): the layout runs in waves of equal chunks, so take the chunk
+  // count per source (up to twice the minimum) with the fewest waves x
+  // tokens per chunk, i.e. the shortest last wave (prefill's 32 x 4096
+  // tokens: 19 chunks of 216 tokens per source, two full waves on 152 SMs,
+  // instead of 16 of 256).
+  int cps = ceil_div(Tr, tr);
+  const long long slots = (long long)num_sms * (E > 256 ? 1 : 2);
+  if ((long long)P * cps > slots) {
+    long long best = -1;
+    const int c0 = cps;
+    for (int c = c0; c <= 2 * c0 && c <= Tr; ++c) {
+      const long long cost = ((long long)P * c + slots - 1) / slots * ceil_div(Tr, c);
+      if (best < 0 || cost < best) {
+        best = cost;
+        cps = c;
+      }
+    }
+    tr = ceil_div(Tr, cps);
+    cps = ceil_div(Tr, tr);
+  }
   p.tpc_route = tr;
-  p.cps_route = ceil_div(Tr, tr);
+  p.cps_route = cps;
   const int n1 = P * p.cps_ids, n2 = P * p.cps_route;
   p.nchunks_max = n1 > n2 ? n1 : n2;
   if (p.nchunks_max < num_sms) p.nchunks_max = num_sms;  // persistent path: one chunk per SM

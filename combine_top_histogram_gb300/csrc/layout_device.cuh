@@ -15,18 +15,12 @@
 namespace moe {
 namespace {
 
-// Lanes of the warp holding the same expert id as this lane (valid ids >= 0),
-// from one ballot per bit of the id: the bit-plane form of a warp multisplit
-// (Ashkiani et al., "GPU Multisplit", PPoPP 2016). Undefined for e < 0.
-__device__ __forceinline__ unsigned peer_mask(int e, int nbits) {
-  unsigned m = __ballot_sync(kFull, e >= 0);
-  for (int b = 0; b < nbits; ++b) {
-    const bool bit = (e >> b) & 1;
-    const unsigned bb = __ballot_sync(kFull, bit);
-    m &= bit ? bb : ~bb;
-  }
-  return m;
-}
+// Lanes of the warp holding the same expert id as this lane (one
+// match.any; a warp multisplit's peer mask, Ashkiani et al., "GPU
+// Multisplit", PPoPP 2016). Lanes with e = -1 match one another; callers
+// use the mask only for valid ids. (An earlier form built it from one
+// ballot per bit of the id: more instructions, and a layout 1-2 us slower.)
+__device__ __forceinline__ unsigned peer_mask(int e) { return __match_any_sync(kFull, e); }
 
 // Order-preserving map of a finite float to an unsigned key (larger float ->
 // larger key); -0 is mapped like +0 so that equal logits tie. Key 0 is below
@@ -142,9 +136,8 @@ __device__ __forceinline__ bool topk_threshold(const unsigned (&key)[EPL], int k
   for (int i = 1; i < EPL; ++i) rest = max(rest, key[i]);
   unsigned tau = 0u;
   int cnt = 0;
-  for (int r = 0; r < k; ++r) {  // warp-uniform
+  for (int r = 0; r < k; ++r) {  // warp-uniform; m == 0 counts every lane and ends it
     const unsigned m = __reduce_max_sync(kFull, rest);
-    if (m == 0u) break;
     cnt += __popc(__ballot_sync(kFull, rest == m));
     if (rest == m) rest = 0u;
     if (cnt >= k) {
@@ -459,12 +452,10 @@ __device__ __forceinline__ void layout_chunk(const LayoutArgs& p, int b, int* sm
   // Pass 1: per-warp expert counts of the warp's contiguous sub-range.
   const int per = (na + kLayoutWarps - 1) / kLayoutWarps;
   const int beg = min(na, warp * per), end = min(na, beg + per);
-  int nbits = 0;
-  while ((1 << nbits) < E) ++nbits;
   for (int base = beg; base < end; base += 32) {
     const int i = base + lane;
     const int e = i < end ? ids_s[i] : -1;
-    const unsigned m = peer_mask(e, nbits);
+    const unsigned m = peer_mask(e);
     if (e >= 0 && lane == __ffs(m) - 1) wcnt[warp * E + e] += __popc(m);
   }
   __syncthreads();
@@ -487,7 +478,7 @@ __device__ __forceinline__ void layout_chunk(const LayoutArgs& p, int b, int* sm
   for (int base = beg; base < end; base += 32) {
     const int i = base + lane;
     const int e = i < end ? ids_s[i] : -1;
-    const unsigned m = peer_mask(e, nbits);
+    const unsigned m = peer_mask(e);
     int code = -1;
     if (e >= 0) code = (e << 16) | (wcnt[warp * E + e] + __popc(m & below));
     __syncwarp();
