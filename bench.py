@@ -467,7 +467,10 @@ def run_ours(args, wl, rank, world, local):
     h2d = x_h.numel() * 2 + sum(t.numel() * t.element_size() for t in r_h)
     d2h = out_h.numel() * 2
     e2e_ms = []
-    eevs = new_events(min(args.steps, 50) + 3)
+    # the first copies from freshly pinned gigabyte buffers run slowly, so the
+    # end-to-end loop warms up for as many steps as the device-timed one
+    e2e_warm = max(3, args.warmup)
+    eevs = new_events(min(args.steps, 50) + e2e_warm)
     for i, ev in enumerate(eevs):
         flush_l2()
         ev[0].record(stream)
@@ -484,7 +487,7 @@ def run_ours(args, wl, rank, world, local):
         B.moe_copy_d2h_async(out_h, layer.out, stream)
         ev[3].record(stream)
     torch.cuda.synchronize(dev)
-    for ev in eevs[3:]:
+    for ev in eevs[e2e_warm:]:
         e2e_ms.append(ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]))
     e2e_us = max_over_ranks(statistics.median(e2e_ms) * 1e3, world)
 
