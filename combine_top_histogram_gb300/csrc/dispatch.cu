@@ -131,18 +131,33 @@ __device__ __forceinline__ void resolve_rows(const DispatchArgs& p, long long g,
 // red[2] | (tables CTAs) sk[E + 32].
 __host__ __device__ constexpr int direct_smem_ints(int E) { return (E + 1) + 32 + 2 + (E + 32); }
 
-// Expert offsets of the layout in eoff[0..E] (kept counts, capacity applied,
-// scanned in global expert order); the writer CTA also stores n_raw, n_kept,
-// expert_offset, rank_base and the layer totals.
-__device__ void direct_offsets(const DispatchArgs& p, int* dsm, bool writer) {
+// The first per-expert totals this thread scans (experts tid and
+// tid + blockDim), loaded into registers ahead of the scan; the scan loads
+// any further ones (E > 2 * blockDim) itself.
+constexpr int kDirectTotalsPerThread = 2;
+__device__ __forceinline__ void direct_totals_load(const DispatchArgs& p,
+                                                   int (&raw)[kDirectTotalsPerThread]) {
+#pragma unroll
+  for (int i = 0; i < kDirectTotalsPerThread; ++i) {
+    const int e = threadIdx.x + i * blockDim.x;
+    raw[i] = e < p.E ? __ldcg(p.acc + e) : 0;
+  }
+}
+
+// The expert offsets from loaded totals (direct_totals_load), as
+// direct_offsets computes them.
+__device__ void direct_offsets_scan(const DispatchArgs& p, int* dsm, bool writer,
+                                    const int (&raw_in)[kDirectTotalsPerThread]) {
   const int E = p.E, tid = threadIdx.x, NT = blockDim.x;
   int* eoff = dsm;
   int* tmp = eoff + E + 1;
   int* red = tmp + 32;
   if (tid < 2) red[tid] = 0;
   int dr = 0, rw = 0;
-  for (int e = tid; e < E; e += NT) {
-    const int raw = __ldcg(p.acc + e);
+  for (int i = 0; tid + i * NT < E; ++i) {
+    const int e = tid + i * NT;
+    static_assert(kDirectTotalsPerThread == 2, "registers named below");
+    const int raw = i == 0 ? raw_in[0] : i == 1 ? raw_in[1] : __ldcg(p.acc + e);
     const int kept = (p.cap > 0 && raw > p.cap) ? p.cap : raw;
     eoff[e] = kept;
     if (writer) {
@@ -172,6 +187,15 @@ __device__ void direct_offsets(const DispatchArgs& p, int* dsm, bool writer) {
   __syncthreads();
 }
 
+// Expert offsets of the layout in eoff[0..E] (kept counts, capacity applied,
+// scanned in global expert order); the writer CTA also stores n_raw, n_kept,
+// expert_offset, rank_base and the layer totals.
+__device__ void direct_offsets(const DispatchArgs& p, int* dsm, bool writer) {
+  int raw[kDirectTotalsPerThread];
+  direct_totals_load(p, raw);
+  direct_offsets_scan(p, dsm, writer, raw);
+}
+
 // Every CTA of a direct-mode launch counts itself out on the arrival counter
 // once it has read the totals for the last time (thread 0's atomic, whose
 // ticket it keeps); the CTA that counted out last clears the totals and the
@@ -197,12 +221,12 @@ __device__ __forceinline__ int load_group_code(const DispatchArgs& p, long long 
   return jt < p.k ? __ldg(p.acode + g * p.k + jt) : -1;
 }
 
-// pre[j] = assignments to slot j's expert that precede token g's chunk: those
-// of earlier sources (acc_se) and of the source's earlier chunks (raw hist),
-// summed over direct_G lanes. Every thread of the CTA takes part (warp-wide
-// shuffles).
-__device__ __forceinline__ void direct_slot_bases(const DispatchArgs& p, long long g, int code,
-                                                  int* pre) {
+// Slot j's assignments to its expert that precede token g's chunk: those of
+// earlier sources (acc_se) and of the source's earlier chunks (raw hist),
+// spread over direct_G lanes; this lane's partial sum (its loads issued as
+// soon as the code is known), then the sum over the lanes into pre[j].
+// Every thread of the CTA takes part in the reduction (warp-wide shuffles).
+__device__ __forceinline__ int direct_slot_terms(const DispatchArgs& p, long long g, int code) {
   const int G = p.direct_G, jt = threadIdx.x / G, li = threadIdx.x - jt * G;
   int sp = 0;
   if (jt < p.k && code >= 0 && row_ok(code_expert(code), p.E, p.status)) {
@@ -213,6 +237,10 @@ __device__ __forceinline__ void direct_slot_bases(const DispatchArgs& p, long lo
     const int32_t* col = p.hist + (long long)e * p.nchunks + (long long)s * p.cps;
     for (int c = li; c < bs; c += G) sp += __ldcg(col + c);
   }
+  return sp;
+}
+__device__ __forceinline__ void direct_slot_reduce(const DispatchArgs& p, int sp, int* pre) {
+  const int G = p.direct_G, jt = threadIdx.x / G, li = threadIdx.x - jt * G;
   for (int o = G >> 1; o > 0; o >>= 1) sp += __shfl_xor_sync(0xffffffffu, sp, o);
   if (li == 0 && jt < p.k) pre[jt] = sp;
 }
@@ -252,12 +280,23 @@ __device__ __forceinline__ void resolve_rows_direct(const DispatchArgs& p, long 
 // the direct mode's expert offsets in shared memory (direct_offsets).
 template <bool DIRECT>
 __device__ __forceinline__ void resolve_token(const DispatchArgs& p, long long g, int* rows_s,
-                                              SlotIn in, int code, const int* eoff) {
+                                              SlotIn& in, int* dsm, bool& offsets_done) {
   if (DIRECT) {
+    // three round trips overlapped: the codes and (first token) the totals
+    // are loaded together, the slot terms as soon as the codes arrive, and
+    // those land while the totals are scanned into the expert offsets
+    in = load_slot(p, g);
+    const int code = load_group_code(p, g);
+    int raw[kDirectTotalsPerThread];
+    const bool first = !offsets_done;
+    if (first) direct_totals_load(p, raw);
+    const int sp = direct_slot_terms(p, g, code);
+    if (first) direct_offsets_scan(p, dsm, false, raw);
+    offsets_done = true;
     __shared__ int pre[MOE_MAX_TOPK];
-    direct_slot_bases(p, g, code, pre);
+    direct_slot_reduce(p, sp, pre);
     __syncthreads();
-    resolve_rows_direct(p, g, rows_s, in, eoff, pre);
+    resolve_rows_direct(p, g, rows_s, in, dsm, pre);
   } else {
     resolve_rows(p, g, rows_s, in);
   }
@@ -317,7 +356,6 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
     // direct mode: the layout kernel is the launch just before, so its codes
     // (and routed weights) are read only after the wait
     SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
-    int gcode = -1;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -333,13 +371,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
           pdl_trigger();
           waited = true;
         }
-        if (DIRECT) {  // the slot loads and (first token) the totals' loads in flight together
-          si = load_slot(p, g);
-          gcode = load_group_code(p, g);
-          if (!offsets_done) direct_offsets(p, dsm, false);
-          offsets_done = true;
-        }
-        resolve_token<DIRECT>(p, g, rows_s, si, gcode, dsm);
+        resolve_token<DIRECT>(p, g, rows_s, si, dsm, offsets_done);
         if (DIRECT && g + nb >= p.T) ticket = direct_count_out(p);  // last read of the totals
         __syncthreads();
       }
@@ -384,7 +416,6 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
     // direct mode: the layout kernel is the launch just before, so its codes
     // (and routed weights) are read only after the wait
     SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
-    int gcode = -1;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -401,13 +432,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
           pdl_trigger();
           waited = true;
         }
-        if (DIRECT) {  // the slot loads and (first token) the totals' loads in flight together
-          si = load_slot(p, g);
-          gcode = load_group_code(p, g);
-          if (!offsets_done) direct_offsets(p, dsm, false);
-          offsets_done = true;
-        }
-        resolve_token<DIRECT>(p, g, rows_s, si, gcode, dsm);
+        resolve_token<DIRECT>(p, g, rows_s, si, dsm, offsets_done);
         if (DIRECT && g + nb >= p.T) ticket = direct_count_out(p);
         __syncthreads();
       }
@@ -465,7 +490,6 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
     // direct mode: the layout kernel is the launch just before, so its codes
     // (and routed weights) are read only after the wait
     SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
-    int gcode = -1;
     const uint16_t* src = p.x + g * p.H;
     for (int c0 = 0; c0 < nch; c0 += CPT * kDispatchThreads) {
       uint4 va[CPT], vb[CPT];
@@ -485,13 +509,7 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
           pdl_trigger();
           waited = true;
         }
-        if (DIRECT) {  // the slot loads and (first token) the totals' loads in flight together
-          si = load_slot(p, g);
-          gcode = load_group_code(p, g);
-          if (!offsets_done) direct_offsets(p, dsm, false);
-          offsets_done = true;
-        }
-        resolve_token<DIRECT>(p, g, rows_s, si, gcode, dsm);
+        resolve_token<DIRECT>(p, g, rows_s, si, dsm, offsets_done);
         if (DIRECT && g + nb >= p.T) ticket = direct_count_out(p);
         __syncthreads();
       }
