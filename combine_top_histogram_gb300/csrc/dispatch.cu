@@ -276,8 +276,9 @@ __device__ __forceinline__ void resolve_rows_direct(const DispatchArgs& p, long 
 }
 
 // The k receive rows of token g into rows_s (either mode); the caller ends
-// with a barrier before reading rows_s. code: load_group_code's value; eoff:
-// the direct mode's expert offsets in shared memory (direct_offsets).
+// with a barrier before reading rows_s. in: the token's slot codes and
+// weights (loaded here in direct mode); dsm: the direct mode's shared memory,
+// whose expert offsets the CTA's first token computes (offsets_done).
 template <bool DIRECT>
 __device__ __forceinline__ void resolve_token(const DispatchArgs& p, long long g, int* rows_s,
                                               SlotIn& in, int* dsm, bool& offsets_done) {
