@@ -352,11 +352,14 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
     return;
   }
   const long long nb = gridDim.x - p.tab_ctas;
+  // the next token's codes and weights are loaded one token ahead (direct
+  // mode: the layout kernel is the launch just before, so its codes are read
+  // only after the wait, in resolve_token)
+  SlotIn si_next = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, p.g0 + blockIdx.x - p.tab_ctas);
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
-    // direct mode: the layout kernel is the launch just before, so its codes
-    // (and routed weights) are read only after the wait
-    SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
+    SlotIn si = si_next;
+    if (!DIRECT && g + nb < p.T) si_next = load_slot(p, g + nb);
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -412,11 +415,14 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8(const Disp
     return;
   }
   const long long nb = gridDim.x - p.tab_ctas;
+  // the next token's codes and weights are loaded one token ahead (direct
+  // mode: the layout kernel is the launch just before, so its codes are read
+  // only after the wait, in resolve_token)
+  SlotIn si_next = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, p.g0 + blockIdx.x - p.tab_ctas);
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
-    // direct mode: the layout kernel is the launch just before, so its codes
-    // (and routed weights) are read only after the wait
-    SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
+    SlotIn si = si_next;
+    if (!DIRECT && g + nb < p.T) si_next = load_slot(p, g + nb);
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -486,11 +492,14 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_fp8w(const Dis
     return;
   }
   const long long nb = gridDim.x - p.tab_ctas;
+  // the next token's codes and weights are loaded one token ahead (direct
+  // mode: the layout kernel is the launch just before, so its codes are read
+  // only after the wait, in resolve_token)
+  SlotIn si_next = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, p.g0 + blockIdx.x - p.tab_ctas);
   for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
-    // direct mode: the layout kernel is the launch just before, so its codes
-    // (and routed weights) are read only after the wait
-    SlotIn si = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, g);
+    SlotIn si = si_next;
+    if (!DIRECT && g + nb < p.T) si_next = load_slot(p, g + nb);
     const uint16_t* src = p.x + g * p.H;
     for (int c0 = 0; c0 < nch; c0 += CPT * kDispatchThreads) {
       uint4 va[CPT], vb[CPT];
