@@ -260,6 +260,53 @@ def test_route_ties_gaps_and_chunkings(gpu, E, k):
         assert oi[0].tolist() == list(range(k))
 
 
+def _threshold_boundary_logits(rng, n_tokens: int, extra: int) -> np.ndarray:
+    """Logits (E = 256) whose top-8 threshold leaves exactly 32 + extra
+    candidate keys: warp lane l holds experts l, l + 32, ..., l + 224, and
+    eight lanes get four large logits each, the last of those lanes four
+    equal ones (so the eighth-largest lane maximum is tied four ways); extra
+    more large logits go to the first lane. Everything else is far below."""
+    E = 256
+    z = rng.standard_normal((n_tokens, E)).astype(np.float32)
+    for t in range(n_tokens):
+        lanes = rng.choice(32, 8, replace=False)
+        regs = [rng.choice(8, 4 + (extra if q == 0 else 0), replace=False) for q in range(8)]
+        tie = np.float32(10.0 + rng.random())
+        for q, (lane, rs) in enumerate(zip(lanes, regs)):
+            for i in rs:
+                z[t, i * 32 + lane] = tie if q == 7 else np.float32(tie + 1.0 + rng.random())
+    return z
+
+
+def test_route_threshold_candidate_boundary(gpu):
+    """The threshold top-k at its candidate limit: exactly 32 candidates (the
+    compacted path, with a four-way tie at the threshold, the lower expert
+    first) and 33 or more (the plain selection instead). Ids exact, weights
+    within 1 fp32 ulp of the double softmax, through the route-only kernel
+    and the fused route + layout."""
+    import torch
+    import oracle
+    from combine_top_histogram_gb300 import MoeLayer
+    from combine_top_histogram_gb300 import binding as B
+    from harness import f32_ulp_diff
+    rng = np.random.default_rng(2026)
+    P, Tr, E, k = 2, 300, 256, 8
+    z = np.concatenate([_threshold_boundary_logits(rng, Tr, 0),
+                        _threshold_boundary_logits(rng, Tr // 2, 1),
+                        _threshold_boundary_logits(rng, Tr - Tr // 2, 4)])
+    oi, ow = oracle.route_topk(z, k)
+    zt = torch.from_numpy(z).cuda()
+    layer = MoeLayer(P, Tr, E, k, 128)
+    ids = torch.empty((P * Tr, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((P * Tr, k), dtype=torch.float32, device="cuda")
+    B.moe_route_topk(layer.handle, zt, ids, w)
+    layer.route_layout(zt)
+    torch.cuda.synchronize()
+    for gi, gw in ((ids, w), (layer.ids, layer.w)):
+        assert np.array_equal(gi.cpu().numpy(), oi)
+        assert f32_ulp_diff(gw.cpu().numpy(), ow).max() <= 1
+
+
 def test_layout_tables_without_dispatch(gpu):
     """The per-source tables (cnt, kept counts, C, send and receive offsets)
     are left to the dispatch launch; moe_layout_tables builds them alone. With
