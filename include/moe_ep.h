@@ -354,8 +354,8 @@ int moe_combine(moe_handle_t h, const void *y, const float *w, void *out,
  * The first call in each device context (the first call on a device, and the
  * first after that device was reset) does a one-time set-up with that device
  * current: it looks up the array's device address and raises the layout
- * kernels' shared-memory limits. Make that first call before any stream
- * capture. Every call shares the array and finds the previous call's
+ * kernels' shared-memory limits (host-side calls, not stream-ordered work).
+ * Every call shares the array and finds the previous call's
  * contents: each call clears the control words first, and calls that overlap
  * on the GPU (other streams, other threads) race and must be serialised by
  * the caller. Ids outside [-1, E) are counted as masked; there is no status
