@@ -355,11 +355,18 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
   // the next token's codes and weights are loaded one token ahead (direct
   // mode: the layout kernel is the launch just before, so its codes are read
   // only after the wait, in resolve_token)
-  SlotIn si_next = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, p.g0 + blockIdx.x - p.tab_ctas);
-  for (long long g = p.g0 + blockIdx.x - p.tab_ctas; g < p.T; g += nb) {
+  const long long gfirst = p.g0 + blockIdx.x - p.tab_ctas;
+  // regular layout: token n's receive rows are resolved during token n-1
+  // (published by token n's barrier), from codes loaded a token before that
+  SlotIn si_next = DIRECT ? SlotIn{-1, 0.0f} : load_slot(p, gfirst);
+  SlotIn si_next2 = (DIRECT || gfirst + nb >= p.T) ? SlotIn{-1, 0.0f} : load_slot(p, gfirst + nb);
+  for (long long g = gfirst; g < p.T; g += nb) {
     int* rows_s = rows_buf[par];
     SlotIn si = si_next;
-    if (!DIRECT && g + nb < p.T) si_next = load_slot(p, g + nb);
+    if (!DIRECT) {
+      si_next = si_next2;
+      if (g + 2 * nb < p.T) si_next2 = load_slot(p, g + 2 * nb);
+    }
     const uint4* src = reinterpret_cast<const uint4*>(p.x + g * p.H);
     for (int v0 = 0; v0 < nvec; v0 += VPT * kDispatchThreads) {
       uint4 val[VPT];
@@ -374,10 +381,12 @@ __global__ void __launch_bounds__(kDispatchThreads, 8) k_dispatch_bf16(const Dis
           pdl_wait();
           pdl_trigger();
           waited = true;
+          if (!DIRECT) resolve_rows(p, g, rows_s, si);  // the CTA's first token
         }
-        resolve_token<DIRECT>(p, g, rows_s, si, dsm, offsets_done);
+        if (DIRECT) resolve_token<DIRECT>(p, g, rows_s, si, dsm, offsets_done);
         if (DIRECT && g + nb >= p.T) ticket = direct_count_out(p);  // last read of the totals
         __syncthreads();
+        if (!DIRECT && g + nb < p.T) resolve_rows(p, g + nb, rows_buf[par ^ 1], si_next);
       }
       for (int j = 0; j < p.k; ++j) {
         const int r = rows_s[j];
